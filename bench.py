@@ -1,0 +1,401 @@
+"""Throughput of the weight-quantized linear layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one call of the layer (qgemm_run) on the workload's synthetic inputs. The
+default workload is the decode GEMV of a 7B-class FFN up-projection: Int4-Block64 weights,
+M=1, K=4096, N=11008, bf16 activations and output. Its metric is the weight-stream
+bandwidth (the layer's algorithmic bytes: packed weights, {offset, scale} table,
+activations in, output out) and, beside it, TFLOPS = 2*M*K*N / t (the benchmark page's
+convention, "MNN GemmSpeed 基准测试实战" «测量流程»).
+
+Timing: weights are packed once (offline, as on the page), then copied into enough
+rotating copies to exceed the L2 cache about 3x, so every call streams its weights from HBM.
+W warm-up calls, then exactly K calls captured in one CUDA graph and replayed between CUDA
+events on the launching stream, with a barrier and synchronize on both sides; the time is
+the max over ranks. GPU clocks are sampled with nvidia-smi during the timed region.
+
+--impl reference times the CPU oracle (float64 plain loops, the test suite's reference) on
+this host's cores on a bounded sample of the same workload; it is a deliberately slow
+baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from weight_quantized_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "qGEMM TFLOPS (2*M*K*N/s) and weight-stream HBM GB/s, % of roofline"
+DEFAULT_WORKLOAD = "int4_b64_decode_m1_k4096_n11008_bf16"
+DTYPE_NAME = {0: "f32", 1: "f16", 2: "bf16"}
+
+
+# ---------------------------------------------------------------- workload accounting
+def algorithmic_bytes(w: synth.Workload) -> int:
+    """Bytes one call must move: packed weights + table + activations in + output out."""
+    esz = {0: 4, 1: 2, 2: 2}
+    if w.mode == synth.MODE_FLOAT:
+        wb = w.K * w.N * esz[w.a_dtype]
+        tb = 0
+    else:
+        wb = w.K * w.N * (4 if w.mode in (synth.MODE_INT4, synth.MODE_W4A8) else 8) // 8
+        blk = w.K if (w.block == 0 or w.mode == synth.MODE_W4A8) else w.block
+        tb = w.N * (w.K // blk) * 8
+    return wb + tb + w.M * w.K * esz[w.a_dtype] + w.M * w.N * esz[w.c_dtype]
+
+
+def bound_of(w: synth.Workload) -> str:
+    return "hbm" if w.M <= 16 else "tensor"
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_quantized_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = src_hash()
+    for ln in open(path):
+        parts = ln.split()
+        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == workload and parts[2] == cur:
+            return int(float(parts[3]))
+    return None
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the oracle arm
+def oracle_step_fn(w: synth.Workload, A, W):
+    """Returns (callable running one bounded oracle sample, units of work per call, description)."""
+    import oracle
+    if w.mode == synth.MODE_FLOAT:
+        Bt = oracle.values(oracle.pack_float(W, w.a_dtype), w.a_dtype)
+        A64 = oracle.values(A, w.a_dtype)
+        rows = max(1, min(w.M, int(2e8 // (w.K * w.N))))
+        return (lambda: oracle.gemm(A64[:rows], Bt)), rows, f"float GEMM of {rows} row(s) of A"
+    qmax = oracle.QMAX[w.mode]
+    blk = w.K if (w.block == 0 or w.mode == synth.MODE_W4A8) else w.block
+    q, T = oracle.quantize(W, blk, qmax)       # offline step, not timed
+    A64 = oracle.values(A, w.a_dtype)
+    if w.mode == synth.MODE_W4A8:
+        rows = max(1, min(w.M, int(4e8 // (w.K * w.N))))
+        A32 = A64[:rows].astype(np.float32)
+
+        def run():
+            qa, s, rs = oracle.act_quant(A32)
+            return oracle.w4a8_out(oracle.w4a8_acc(qa, q), s, rs, T)
+        return run, rows, f"W4A8 on {rows} row(s) of A"
+    rows = max(1, min(w.M, int(4e8 // (w.K * w.N))))
+
+    def run():
+        return oracle.gemm(A64[:rows], oracle.dequant(q, T, blk))
+    return run, rows, f"dequant + float64 GEMM of {rows} row(s) of A"
+
+
+def run_reference(args, w: synth.Workload) -> dict:
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    oracle.set_threads(threads)
+    A = synth.make_activations(w)
+    W = synth.make_weights(w)
+    fn, rows, desc = oracle_step_fn(w, A, W)
+    for _ in range(max(1, min(args.warmup, 1))):
+        fn()
+    steps = max(1, args.steps)
+    budget = getattr(args, "cpu_seconds", 60.0)
+    t0 = time.perf_counter()
+    done = 0
+    while done < steps:
+        fn()
+        done += 1
+        if time.perf_counter() - t0 > budget:    # bound the CPU arm's run time
+            break
+    dt = (time.perf_counter() - t0) / done
+    frac = rows / w.M
+    bytes_per = algorithmic_bytes(w) * frac
+    value = bytes_per / dt / 1e9
+    return {"value": value, "unit": "GB/s", "ms_per_step": dt * 1e3, "steps": done, "cores": oracle.set_threads(0),
+            "sample": f"{desc} of {w.name} per step ({frac:.3g} of the layer), {done} step(s)",
+            "tflops": 2.0 * rows * w.K * w.N / dt / 1e12}
+
+
+# ---------------------------------------------------------------- the GPU arm
+def to_torch(arr: np.ndarray, code: int, device):
+    import torch
+    if code == synth.BF16:
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+    return t.to(device)
+
+
+def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
+    import torch
+
+    import weight_quantized_gemm_gb300 as qg
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
+    A_np = synth.make_activations(w)
+    W_np = synth.make_weights(w)
+    K, N, M = w.K, w.N, w.M
+    with torch.cuda.stream(stream):
+        A = to_torch(A_np, w.a_dtype, device)
+        Wd = torch.from_numpy(W_np).to(device)
+        pb = qg.qgemm_packed_bytes(K, N, w.mode, w.w_dtype if w.mode == 0 else 0)
+        tb = qg.qgemm_table_bytes(K, N, w.mode, w.block)
+        Bp0 = torch.empty(pb, dtype=torch.uint8, device=device)
+        T0 = torch.empty(max(tb // 4, 4), dtype=torch.float32, device=device)
+        qg.qgemm_pack(Wd, K, N, w.mode, w.block, w.a_dtype if w.mode == 0 else 0, Bp0, T0 if tb else None,
+                      stream=stream)
+        del Wd
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        copy_bytes = pb + tb
+        copies = max(2, -(-3 * l2 // max(copy_bytes, 1)))
+        Bps = [Bp0] + [Bp0.clone() for _ in range(copies - 1)]
+        Ts = [T0] + [T0.clone() for _ in range(copies - 1)]
+        C = torch.empty((M, N), dtype=tdt[w.c_dtype], device=device)
+        wsb = qg.qgemm_workspace_bytes(M, K, N, w.mode, w.block, w.a_dtype, w.c_dtype)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+    stream.synchronize()
+    s_ptr = stream.cuda_stream
+    lib = qg.load()
+
+    def call(i):
+        rc = lib.qgemm_run(M, K, N, w.mode, w.block, A.data_ptr(), w.a_dtype, Bps[i % copies].data_ptr(),
+                           Ts[i % copies].data_ptr() if tb else None, C.data_ptr(), w.c_dtype, ws.data_ptr(), wsb,
+                           s_ptr)
+        if rc != 0:
+            raise qg.QgemmError(rc, "qgemm_run")
+
+    launches_per_call = 1 + (1 if (w.mode == synth.MODE_W4A8) else 0)
+    # warm-up (eager) and graph capture of exactly K calls
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(args.steps):
+            call(i)
+    stream.synchronize()
+    graph.replay()          # one untimed replay: the graph's own first-launch cost stays out
+    stream.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            graph.replay()
+            end.record(stream)
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        if t_wall < 1.0:    # keep the sampler running long enough to see the load (replays are identical)
+            reps = int(1.0 / max(t_wall, 1e-4))
+            with torch.cuda.stream(stream):
+                for _ in range(min(reps, 2000)):
+                    graph.replay()
+            stream.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    # end to end through the public API with host buffers: H2D of A, the call, D2H of C, per step
+    A_host = A.cpu().pin_memory()
+    C_host = torch.empty(C.shape, dtype=C.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 300))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            A.copy_(A_host, non_blocking=True)
+            qg.qgemm_run(M, K, N, w.mode, w.block, A, w.a_dtype, Bps[i % copies], Ts[i % copies] if tb else None, C,
+                         w.c_dtype, ws if wsb else None, wsb, stream=stream)
+            C_host.copy_(C, non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    return {"ms": ms, "clocks": clocks, "copies": copies, "copy_bytes": copy_bytes, "l2": l2,
+            "launches_per_call": launches_per_call, "e2e_s": e2e_s,
+            "h2d": A.numel() * A.element_size(), "d2h": C.numel() * C.element_size()}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    peaks = load_peaks()
+    base_config = {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "mode": synth.MODE_NAMES[w.mode],
+                   "block": w.block if w.block else w.K, "a_dtype": DTYPE_NAME[w.a_dtype],
+                   "c_dtype": DTYPE_NAME[w.c_dtype]}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        r = run_reference(args, w)
+        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": r["unit"], "n_gpus": args.gpus,
+                "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": base_config, "tflops": r["tflops"],
+                "cpu_baseline": {"value": r["value"], "unit": r["unit"], "cores": r["cores"], "kind": "oracle",
+                                 "sample": r["sample"]},
+                "e2e": {"value": r["value"], "unit": r["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = dist_mod
+    r = run_gpu(args, w, rank, world, dist)
+    step_s = r["ms"] / 1e3 / args.steps
+    alg = algorithmic_bytes(w)
+    gbs = alg / step_s / 1e9 * world
+    tflops = w.flops / step_s / 1e12 * world
+    bound = bound_of(w)
+    if bound == "hbm":
+        achieved, peak, unit = alg / step_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = w.flops / step_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    line = {
+        "metric": METRIC, "value": gbs if bound == "hbm" else tflops, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.a_dtype],
+        "data": "synthetic (seeded SplitMix64/Box-Muller inputs of the workload's shape)",
+        "config": dict(base_config, parallelism=f"replicas x{world}",
+                       l2=f"{r['copies']} rotating weight copies of {r['copy_bytes'] / 1e6:.1f} MB "
+                          f"(> 3x the {r['l2'] / 1e6:.0f} MB L2)",
+                       timing=f"CUDA graph of {args.steps} back-to-back calls, CUDA events"),
+        "tflops": tflops, "gbs": gbs,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+                     "traffic": measured_traffic(w.name), "algorithmic_bytes": alg},
+        "clocks": r["clocks"], "gpu_launches": args.steps * r["launches_per_call"],
+        "e2e": {"value": (alg / r["e2e_s"] / 1e9) if bound == "hbm" else (w.flops / r["e2e_s"] / 1e12),
+                "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "ms_per_step": r["e2e_s"] * 1e3,
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        ra = argparse.Namespace(steps=10 ** 6, warmup=1, cpu_seconds=10.0)
+        ref = run_reference(ra, w)
+        line["cpu_baseline"] = {"value": ref["value"], "unit": ref["unit"], "cores": ref["cores"], "kind": "oracle",
+                                "sample": ref["sample"]}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,141 @@
+/*
+ * qgemm: weight-quantized linear layer C[M,N] = A[M,K] x dequant(B[K,N]) on NVIDIA GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The operation and its formats follow the benchmark page "MNN GemmSpeed 基准测试实战：多后端
+ * LLM GEMM 吞吐评估与 GPU 时间戳剖析":
+ *   - «为什么用 Conv1x1 来测 GEMM»: the LLM linear layer is C = A[M,K] x B[K,N] with the
+ *     weight given as {ic, oc} = {K, N}; quantized weights are asymmetric with one
+ *     [offset, scale] pair per (output channel, K-block), stored as oc x blockNum pairs;
+ *     Int8-Block0 is 8-bit with one block over all of K, Int4-Block64 is 4-bit with blocks
+ *     of 64 along K (K % 64 == 0 is required).
+ *   - «测试用例与注册机制»: mode numbers 0 float, 1 Int4-Block64, 2 Int8-Block0, 3 W4A8
+ *     (per-channel INT4 weights unpacked to INT8, activations dynamically quantized to
+ *     INT8, S8 x S8 -> S32 accumulation).
+ *   - «测量流程»: throughput is counted as 2*M*K*N flops per call.
+ *
+ * Conventions for every function below:
+ *   - All buffer pointers are DEVICE pointers owned by the caller (allocate them with any
+ *     allocator; the library never allocates, frees or retains them). Each must be 16-byte
+ *     aligned; 128-byte alignment is recommended.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Compute
+ *     calls only enqueue work and return; results are ready once the stream is synchronized.
+ *   - Return value: QGEMM_OK (0) or a negative QGEMM_ERR_* code. Every argument is checked
+ *     before anything is launched; on an error nothing is enqueued and no buffer is written.
+ *     qgemm_last_error() gives a one-line description of the last error on this thread.
+ *   - Sizes are int; products of sizes are computed in 64 bits.
+ *
+ * Layouts (row-major unless stated):
+ *   W   float32 [K][N]            the unquantized weight, {ic, oc} = {K, N}
+ *   Bp  packed weight, output-channel-major with K contiguous:
+ *         INT4 / W4A8  uint8 [N][K/2], byte j of a row = q[2j] | q[2j+1] << 4
+ *         INT8         uint8 [N][K]
+ *         FLOAT        [N][K] in the activation dtype (f16, bf16 or f32)
+ *   T   float32 [N][K/block][2] = {offset, scale} per (channel, block); absent in FLOAT mode
+ *   A   [M][K] in a_dtype;  C  [M][N] in c_dtype
+ * Dequantization: w[k][n] = q[n][k] * scale[n][k/block] + offset[n][k/block], with unsigned
+ * codes q in [0, 15] (4-bit) or [0, 255] (8-bit).
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* weight formats (same numbering as the benchmark page's mode column) */
+#define QGEMM_MODE_FLOAT 0 /* unquantized 16/32-bit weight                       */
+#define QGEMM_MODE_INT4 1  /* asymmetric 4-bit, block = 64 (any multiple of 64)  */
+#define QGEMM_MODE_INT8 2  /* asymmetric 8-bit, block = K (Block0) or multiple of 64 */
+#define QGEMM_MODE_W4A8 3  /* per-channel 4-bit weight x dynamic per-row 8-bit activation */
+
+/* element types */
+#define QGEMM_F32 0
+#define QGEMM_F16 1
+#define QGEMM_BF16 2
+
+/* status codes */
+#define QGEMM_OK 0
+#define QGEMM_ERR_ARG (-1)         /* null pointer, negative size, unknown mode or dtype        */
+#define QGEMM_ERR_UNSUPPORTED (-2) /* K % 64 != 0, K % block != 0, block not a multiple of 64,
+                                      W4A8 with block != K, FLOAT weights of another dtype,
+                                      a size beyond the launch limits                          */
+#define QGEMM_ERR_ALIGN (-3)       /* a pointer is not 16-byte aligned                          */
+#define QGEMM_ERR_WORKSPACE (-4)   /* workspace smaller than qgemm_workspace_bytes()            */
+#define QGEMM_ERR_CUDA (-5)        /* a CUDA call or launch failed (detail in qgemm_last_error) */
+#define QGEMM_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait (reported by qgemm_status) */
+
+/* ---------------------------------------------------------------- sizes (host only, no GPU needed) */
+
+/* Bytes of the packed weight Bp for a K x N layer. FLOAT mode stores w_dtype elements; the
+ * quantized modes ignore w_dtype. Returns 0 for invalid arguments. */
+size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype);
+
+/* Bytes of the {offset, scale} table T (0 in FLOAT mode or for invalid arguments).
+ * block = 0 means one block over all of K. */
+size_t qgemm_table_bytes(int K, int N, int mode, int block);
+
+/* Bytes of scratch device memory qgemm_run needs for this call (0 if none). The decode
+ * path needs it only when it splits K across thread blocks (small N); W4A8 needs it for the
+ * quantized activations (M*K bytes of codes, M scales and M row sums). */
+size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype);
+
+/* ---------------------------------------------------------------- weight preparation */
+
+/* Quantize and pack a float32 weight W [K][N] (benchmark page «为什么用 Conv1x1 来测 GEMM»).
+ * For each channel n and block b (block elements along K), in float32 round-to-nearest:
+ *   lo = min w, hi = max w, scale = (hi - lo) / qmax, offset = lo,
+ *   q = clamp(rint((w - lo) / scale), 0, qmax) with ties to even; q = 0 if scale == 0.
+ * qmax = 15 for INT4 and W4A8, 255 for INT8. W4A8 requires block = 0 (per channel).
+ * FLOAT mode instead writes W transposed to [N][K], rounded to nearest-even in w_dtype,
+ * and T may be NULL. W must be finite. Writes Bp (qgemm_packed_bytes) and T
+ * (qgemm_table_bytes). */
+int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, void* Bp, float* T,
+               void* stream);
+
+/* ---------------------------------------------------------------- the layer */
+
+/* C = A x dequant(Bp, T) for modes 0-3 (the operation of the benchmark page's four test
+ * cases, «测试用例与注册机制»).
+ *   a_dtype: f32, f16 or bf16. FLOAT mode expects Bp in the same dtype as A.
+ *   c_dtype: f32, f16 or bf16 (results are accumulated in f32 and rounded once).
+ *   W4A8: A is quantized per row (as = max|a| / 127, qa = clamp(rint(a / as), -127, 127)),
+ *   acc = sum_k qa * q in int32, and C = as * (ws * acc + off * sum_k qa).
+ * Kernel choice is by shape only: f32 activations use an exact CUDA-core kernel; M <= 16
+ * uses the weight-streaming decode kernel; larger M uses the tensor-core (tcgen05) kernel.
+ * workspace may be NULL when qgemm_workspace_bytes() returns 0. M == 0 or N == 0 is a valid
+ * empty call that launches nothing. */
+int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+              const float* T, void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The W4A8 activation step alone (same page and section: "激活动态量化为 INT8"): per row of
+ * A [M][K], as[m] = max|a| / 127 (float32), qa = clamp(rint(a / as), -127, 127) with ties
+ * to even (all 0 when as == 0), rowsum[m] = sum_k qa. Outputs qa int8 [M][K], as float32 [M],
+ * rowsum int32 [M]. */
+int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* a_scale, int32_t* rowsum,
+                    void* stream);
+
+/* The W4A8 integer GEMM alone ("S8×S8→S32"): acc[m][n] = sum_k qa[m][k] * q[n][k] with q the
+ * 4-bit codes of Bp [N][K/2] read as int8 values 0..15. Writes acc int32 [M][N]. */
+int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* stream);
+
+/* ---------------------------------------------------------------- status */
+
+/* Synchronize `stream`, then report (and clear) the library's device status word: QGEMM_OK,
+ * QGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait, or QGEMM_ERR_CUDA. */
+int qgemm_status(void* stream);
+
+/* Static name of a status code. */
+const char* qgemm_error_string(int code);
+
+/* Description of the last error returned on the calling thread ("" if none). */
+const char* qgemm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

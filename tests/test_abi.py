@@ -1,0 +1,100 @@
+"""The C ABI without a GPU: the library loads, exports every function include/qgemm.h
+declares, sizes are right, and every argument check returns its code before any launch."""
+import ctypes
+import subprocess
+
+import pytest
+
+from tests._util import header_functions, ensure_built
+
+import weight_quantized_gemm_gb300 as qg
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ensure_built()
+
+
+def test_exports_every_declared_symbol():
+    names = header_functions()
+    assert {"qgemm_pack", "qgemm_run", "qgemm_workspace_bytes", "qgemm_status"} <= set(names)
+    lib = ctypes.CDLL(qg.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", qg.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert set(names) <= exported
+    assert set(names) == set(qg.SIGNATURES)          # the binding covers exactly the header
+
+
+def test_sizes():
+    assert qg.qgemm_packed_bytes(4096, 11008, qg.MODE_INT4) == 4096 * 11008 // 2
+    assert qg.qgemm_table_bytes(4096, 11008, qg.MODE_INT4, 64) == 11008 * 64 * 8
+    assert qg.qgemm_packed_bytes(4096, 4096, qg.MODE_INT8) == 4096 * 4096
+    assert qg.qgemm_table_bytes(4096, 4096, qg.MODE_INT8, 0) == 4096 * 8
+    assert qg.qgemm_packed_bytes(256, 512, qg.MODE_FLOAT, qg.F16) == 256 * 512 * 2
+    assert qg.qgemm_packed_bytes(256, 512, qg.MODE_FLOAT, qg.F32) == 256 * 512 * 4
+    assert qg.qgemm_table_bytes(256, 512, qg.MODE_FLOAT, 0) == 0
+    assert qg.qgemm_packed_bytes(100, 512, qg.MODE_INT4) == 0           # K % 64 != 0
+    assert qg.qgemm_table_bytes(256, 512, qg.MODE_INT4, 96) == 0       # block not a multiple of 64
+    # W4A8: qa (M*K bytes), scales and row sums, each 256-byte aligned
+    assert qg.qgemm_workspace_bytes(2048, 4096, 14336, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == 2048 * 4096 + 2 * 8192
+    # decode with a large N needs no scratch; a small N splits K across blocks
+    assert qg.qgemm_workspace_bytes(1, 4096, 11008, qg.MODE_INT4, 64, qg.BF16, qg.BF16) == 0
+    assert qg.qgemm_workspace_bytes(1, 4096, 512, qg.MODE_INT4, 64, qg.BF16, qg.BF16) > 0
+
+
+FAKE = 1 << 40          # 16-byte aligned addresses that are never dereferenced (calls fail first)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(K=100), -2),                      # K % 64
+    (dict(block=96), -2),                   # block not a multiple of 64
+    (dict(block=128, K=192), -2),           # K % block
+    (dict(mode=7), -1),
+    (dict(a_dtype=5), -1),
+    (dict(c_dtype=-1), -1),
+    (dict(M=-1), -1),
+    (dict(K=0), -1),
+    (dict(A=0), -1),
+    (dict(T=0), -1),
+    (dict(C=FAKE + 8), -3),                 # misaligned
+    (dict(Bp=FAKE + 1), -3),
+    (dict(mode=3, block=64), -2),           # W4A8 is per channel
+    (dict(mode=3, block=0, ws=0, ws_bytes=0), -4),   # W4A8 needs scratch for the activation codes
+    (dict(N=512, ws=0, ws_bytes=0), -4),    # small N: split-K scratch needed
+    (dict(M=1 << 21), -2),                  # beyond the launch limit
+])
+def test_run_rejects_before_launch(args, code):
+    a = dict(M=1, K=4096, N=11008, mode=1, block=64, A=FAKE, a_dtype=2, Bp=FAKE, T=FAKE, C=FAKE, c_dtype=2,
+             ws=FAKE, ws_bytes=0, stream=0)
+    a.update(args)
+    rc = qg.load().qgemm_run(a["M"], a["K"], a["N"], a["mode"], a["block"], a["A"], a["a_dtype"], a["Bp"], a["T"],
+                             a["C"], a["c_dtype"], a["ws"], a["ws_bytes"], a["stream"])
+    assert rc == code, qg.qgemm_last_error()
+    assert qg.qgemm_last_error() != ""
+
+
+def test_empty_calls_are_noops():
+    lib = qg.load()
+    assert lib.qgemm_run(0, 4096, 64, 1, 64, None, 2, None, None, None, 2, None, 0, None) == 0
+    assert lib.qgemm_run(4, 4096, 0, 1, 64, None, 2, None, None, None, 2, None, 0, None) == 0
+    assert lib.qgemm_act_quant(0, 4096, None, 2, None, None, None, None) == 0
+    assert lib.qgemm_pack(None, 4096, 0, 1, 64, 0, None, None, None) == 0
+
+
+def test_pack_and_aux_reject():
+    lib = qg.load()
+    assert lib.qgemm_pack(FAKE, 4096, 64, 1, 64, 0, FAKE, None, None) == -1          # null T
+    assert lib.qgemm_pack(FAKE + 4, 4096, 64, 1, 64, 0, FAKE, FAKE, None) == -3      # misaligned W
+    assert lib.qgemm_pack(FAKE, 4096, 64, 0, 0, 9, FAKE, None, None) == -1           # bad w_dtype
+    assert lib.qgemm_pack(FAKE, 4096, 64, 3, 64, 0, FAKE, FAKE, None) == -2          # W4A8 per channel
+    assert lib.qgemm_act_quant(4, 100, FAKE, 2, FAKE, FAKE, FAKE, None) == -2
+    assert lib.qgemm_act_quant(4, 128, FAKE, 2, FAKE + 2, FAKE, FAKE, None) == -3
+    assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, None) == -1
+
+
+def test_error_strings():
+    for code, name in qg.ERRORS.items():
+        assert qg.qgemm_error_string(code) == name
+    assert qg.qgemm_error_string(0) == "QGEMM_OK"

@@ -1,0 +1,135 @@
+"""Python binding of libqgemm (include/qgemm.h): the same entry points, argument marshalling only.
+
+Every compute step runs in the library's CUDA kernels; this module only turns torch tensors
+into device pointers and the current CUDA stream into a cudaStream_t. It never falls back to
+a CPU or PyTorch implementation: if the compiled library is missing, importing the binding
+functions raises.
+
+Build the library with ``__graft_entry__.build()`` (or ``python -m weight_quantized_gemm_gb300._build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
+    "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
+    "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
+]
+
+MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
+F32, F16, BF16 = 0, 1, 2
+OK = 0
+ERRORS = {-1: "QGEMM_ERR_ARG", -2: "QGEMM_ERR_UNSUPPORTED", -3: "QGEMM_ERR_ALIGN", -4: "QGEMM_ERR_WORKSPACE",
+          -5: "QGEMM_ERR_CUDA", -6: "QGEMM_ERR_TIMEOUT"}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemm.so")
+_lib = None
+
+# exported symbol -> (argtypes, restype)
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "qgemm_packed_bytes": ([_I, _I, _I, _I], _SZ),
+    "qgemm_table_bytes": ([_I, _I, _I, _I], _SZ),
+    "qgemm_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "qgemm_pack": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "qgemm_run": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _SZ, _P], _I),
+    "qgemm_act_quant": ([_I, _I, _P, _I, _P, _P, _P, _P], _I),
+    "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P], _I),
+    "qgemm_status": ([_P], _I),
+    "qgemm_error_string": ([_I], ctypes.c_char_p),
+    "qgemm_last_error": ([], ctypes.c_char_p),
+}
+
+
+class QgemmError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = code
+        detail = load().qgemm_last_error().decode(errors="replace")
+        super().__init__(f"{fn}: {ERRORS.get(code, code)}: {detail}")
+
+
+def load():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libqgemm is not built ({LIB_PATH} missing); run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    """Device (or host) address of a tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, fn: str):
+    if rc != OK:
+        raise QgemmError(rc, fn)
+
+
+# ---------------------------------------------------------------- sizes
+def qgemm_packed_bytes(K: int, N: int, mode: int, w_dtype: int = F16) -> int:
+    return load().qgemm_packed_bytes(K, N, mode, w_dtype)
+
+
+def qgemm_table_bytes(K: int, N: int, mode: int, block: int) -> int:
+    return load().qgemm_table_bytes(K, N, mode, block)
+
+
+def qgemm_workspace_bytes(M: int, K: int, N: int, mode: int, block: int, a_dtype: int, c_dtype: int) -> int:
+    return load().qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, c_dtype)
+
+
+# ---------------------------------------------------------------- compute
+def qgemm_pack(W, K: int, N: int, mode: int, block: int, w_dtype: int, Bp, T, stream=None) -> None:
+    _check(load().qgemm_pack(_ptr(W), K, N, mode, block, w_dtype, _ptr(Bp), _ptr(T), _stream(stream)), "qgemm_pack")
+
+
+def qgemm_run(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, C, c_dtype: int,
+              workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().qgemm_run(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(C), c_dtype,
+                            _ptr(workspace), workspace_bytes, _stream(stream)), "qgemm_run")
+
+
+def qgemm_act_quant(M: int, K: int, A, a_dtype: int, qa, a_scale, rowsum, stream=None) -> None:
+    _check(load().qgemm_act_quant(M, K, _ptr(A), a_dtype, _ptr(qa), _ptr(a_scale), _ptr(rowsum), _stream(stream)),
+           "qgemm_act_quant")
+
+
+def qgemm_w4a8_acc(M: int, K: int, N: int, qa, Bp, acc, stream=None) -> None:
+    _check(load().qgemm_w4a8_acc(M, K, N, _ptr(qa), _ptr(Bp), _ptr(acc), _stream(stream)), "qgemm_w4a8_acc")
+
+
+def qgemm_status(stream=None) -> int:
+    return load().qgemm_status(_stream(stream))
+
+
+def qgemm_error_string(code: int) -> str:
+    return load().qgemm_error_string(code).decode()
+
+
+def qgemm_last_error() -> str:
+    return load().qgemm_last_error().decode(errors="replace")

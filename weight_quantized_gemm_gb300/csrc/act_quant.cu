@@ -1,0 +1,109 @@
+// W4A8 activation step: dynamic per-row symmetric INT8 quantization of A.
+//
+// Benchmark page "MNN GemmSpeed 基准测试实战", «测试用例与注册机制»: the W4A8 path quantizes the
+// activations dynamically to INT8. Per row, in float32: as = max|a| / 127, qa = clamp(rint(a / as),
+// -127, 127) with ties to even (qa = 0 when as == 0), rowsum = sum qa. The division is the
+// correctly rounded IEEE one, so the codes match any IEEE float32 evaluation bit for bit.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace qg {
+namespace {
+
+constexpr int kThreads = 256;
+
+// 8 consecutive activations as float32
+template <int ADT>
+__device__ __forceinline__ void load8(const void* A, size_t i, float (&v)[8]) {
+    if constexpr (ADT == DT_F32) {
+        const float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(A) + i);
+        const float4 y = *reinterpret_cast<const float4*>(static_cast<const float*>(A) + i + 4);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    } else {
+        const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(A) + i);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (ADT == DT_BF16) {
+                v[2 * j] = __uint_as_float(w[j] << 16);
+                v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            } else {
+                v[2 * j] = __half2float(__ushort_as_half((unsigned short)(w[j] & 0xFFFFu)));
+                v[2 * j + 1] = __half2float(__ushort_as_half((unsigned short)(w[j] >> 16)));
+            }
+        }
+    }
+}
+
+template <int ADT>
+__global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* __restrict__ A,
+                                                             int8_t* __restrict__ qa, float* __restrict__ as,
+                                                             int32_t* __restrict__ rowsum) {
+    __shared__ float s_max[kThreads / 32];
+    __shared__ int s_sum[kThreads / 32];
+    const int m = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t row = (size_t)m * K;
+
+    float amax = 0.f;
+    for (int k = threadIdx.x * 8; k < K; k += kThreads * 8) {
+        float v[8];
+        load8<ADT>(A, row + k, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) s_max[warp] = amax;
+    __syncthreads();
+    amax = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+
+    int sum = 0;
+    for (int k = threadIdx.x * 8; k < K; k += kThreads * 8) {
+        float v[8];
+        load8<ADT>(A, row + k, v);
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int c = 0;
+            if (s != 0.f) {
+                c = __float2int_rn(__fdiv_rn(v[j], s));
+                c = c < -127 ? -127 : (c > 127 ? 127 : c);
+            }
+            sum += c;
+            packed[j >> 2] |= (uint32_t)(c & 0xFF) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint2*>(qa + row + k) = make_uint2(packed[0], packed[1]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) s_sum[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) total += s_sum[w];
+        as[m] = s;
+        rowsum[m] = total;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* as, int32_t* rowsum,
+                             cudaStream_t s) {
+    if (a_dtype == DT_F32)
+        act_quant_kernel<DT_F32><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+    else if (a_dtype == DT_F16)
+        act_quant_kernel<DT_F16><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+    else
+        act_quant_kernel<DT_BF16><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -1,0 +1,74 @@
+// Internal launch interface between the C ABI (qgemm_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qg {
+
+enum Fmt { FMT_FLOAT = 0, FMT_INT4 = 1, FMT_INT8 = 2 };
+enum Dt { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
+
+inline size_t dt_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+// SM count the grid heuristics are sized for (GB300: 152 SMs). A constant, so that host-side
+// size queries (workspace bytes) give the same answer with or without a GPU present.
+constexpr int kTargetSms = 152;
+
+// ---------------------------------------------------------------- pack
+cudaError_t launch_quant_pack(const float* W, int K, int N, int block, int nbits, uint8_t* Bp, float* T,
+                              cudaStream_t s);
+cudaError_t launch_float_pack(const float* W, int K, int N, int w_dtype, void* Bp, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode (M small)
+struct DecodeArgs {
+    int M, K, N;
+    int block;        // K-group size of the table (multiple of 64; == K for per-channel)
+    int fmt;          // Fmt
+    int a_dtype;      // DT_F16 / DT_BF16 for the tensor-core decode; any for the f32 kernel
+    int c_dtype;
+    const void* A;
+    const void* Bp;
+    const float* T;
+    void* C;
+    float* partial;   // [splits][M][N] f32 partial sums when splits > 1
+    int splits;       // number of K-splits across thread blocks (>= 1)
+};
+// K-splits the decode kernel uses for this shape (1 = none).
+int decode_splits(int M, int K, int N);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// Exact float32 CUDA-core kernel (any activation dtype, any M); used for f32 activations.
+cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- prefill / W4A8
+struct PrefillArgs {
+    int M, K, N, block, fmt, a_dtype, c_dtype;
+    const void* A;
+    const void* Bp;
+    const float* T;
+    void* C;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+bool prefill_supported(int M, int K, int N, int fmt, int a_dtype);
+
+cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* as, int32_t* rowsum,
+                             cudaStream_t s);
+// acc (int32 [M][N]) = qa x q^T; or, when acc == nullptr, the rescaled output into C.
+struct W4A8Args {
+    int M, K, N;
+    const int8_t* qa;
+    const float* as;
+    const int32_t* rowsum;
+    const void* Bp;
+    const float* T;
+    int32_t* acc;   // int32 accumulators out (or nullptr)
+    void* C;        // rescaled output (or nullptr)
+    int c_dtype;
+};
+cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
+
+// device status word (bounded waits that gave up); read and cleared by qgemm_status
+cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+
+}  // namespace qg

@@ -1,0 +1,221 @@
+// The C ABI of include/qgemm.h: argument checks, workspace sizing and kernel choice.
+// Every check runs before the first launch, so a rejected call enqueues nothing.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "../../include/qgemm.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(QGEMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_dtype(int d) { return d == QGEMM_F32 || d == QGEMM_F16 || d == QGEMM_BF16; }
+bool valid_mode(int m) { return m >= QGEMM_MODE_FLOAT && m <= QGEMM_MODE_W4A8; }
+
+// Checks shared by pack and run; `block` is normalised (0 -> K). Returns QGEMM_OK or a code.
+int check_shape(int K, int N, int mode, int* block) {
+    if (!valid_mode(mode)) return fail(QGEMM_ERR_ARG, "unknown mode %d", mode);
+    if (K <= 0 || N < 0) return fail(QGEMM_ERR_ARG, "invalid sizes K=%d N=%d", K, N);
+    if (K % 64 != 0) return fail(QGEMM_ERR_UNSUPPORTED, "K=%d is not a multiple of 64", K);
+    if (*block < 0) return fail(QGEMM_ERR_ARG, "negative block %d", *block);
+    if (*block == 0) *block = K;
+    if (mode == QGEMM_MODE_FLOAT) return QGEMM_OK;
+    if (*block % 64 != 0 || K % *block != 0)
+        return fail(QGEMM_ERR_UNSUPPORTED, "block %d must be a multiple of 64 dividing K=%d", *block, K);
+    if (mode == QGEMM_MODE_W4A8 && *block != K)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A8 weights are per channel (block = K), got block %d", *block);
+    return QGEMM_OK;
+}
+
+size_t packed_bytes(int K, int N, int mode, int w_dtype) {
+    switch (mode) {
+        case QGEMM_MODE_FLOAT: return (size_t)K * N * qg::dt_size(w_dtype);
+        case QGEMM_MODE_INT8: return (size_t)K * N;
+        default: return (size_t)K * N / 2;
+    }
+}
+
+// W4A8 workspace: qa [M][K] int8, then as [M] f32 and rowsum [M] int32, each 256-B aligned.
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t w4a8_ws(int M, int K) { return align256((size_t)M * K) + align256((size_t)M * 4) * 2; }
+
+// Kernel choice by shape (one backend: these are all this library's CUDA kernels).
+enum Path { PATH_F32, PATH_DECODE, PATH_PREFILL };
+Path choose_path(int M, int K, int N, int mode, int a_dtype) {
+    if (a_dtype == QGEMM_F32) return PATH_F32;
+    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
+    if (M > 16 && qg::prefill_supported(M, K, N, fmt, a_dtype)) return PATH_PREFILL;
+    return PATH_DECODE;
+}
+
+size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype) {
+    if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K);
+    if (choose_path(M, K, N, mode, a_dtype) != PATH_DECODE) return 0;
+    const int splits = qg::decode_splits(M, K, N);
+    return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    (void)block;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype) {
+    int block = 0;
+    if (check_shape(K, N, mode, &block) != QGEMM_OK) return 0;
+    if (mode == QGEMM_MODE_FLOAT && !valid_dtype(w_dtype)) return 0;
+    return packed_bytes(K, N, mode, w_dtype);
+}
+
+size_t qgemm_table_bytes(int K, int N, int mode, int block) {
+    if (check_shape(K, N, mode, &block) != QGEMM_OK || mode == QGEMM_MODE_FLOAT) return 0;
+    return (size_t)N * (K / block) * 2 * sizeof(float);
+}
+
+size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype) {
+    if (M <= 0 || check_shape(K, N, mode, &block) != QGEMM_OK || !valid_dtype(a_dtype) || !valid_dtype(c_dtype))
+        return 0;
+    return run_ws(M, K, N, mode, block, a_dtype);
+}
+
+int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, void* Bp, float* T, void* stream) {
+    int rc = check_shape(K, N, mode, &block);
+    if (rc != QGEMM_OK) return rc;
+    if (N == 0) return QGEMM_OK;
+    if (!W || !Bp) return fail(QGEMM_ERR_ARG, "null W or Bp");
+    if (!aligned16(W) || !aligned16(Bp)) return fail(QGEMM_ERR_ALIGN, "W and Bp must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == QGEMM_MODE_FLOAT) {
+        if (!valid_dtype(w_dtype)) return fail(QGEMM_ERR_ARG, "unknown w_dtype %d", w_dtype);
+        e = qg::launch_float_pack(W, K, N, w_dtype, Bp, s);
+    } else {
+        if (!T) return fail(QGEMM_ERR_ARG, "null T");
+        if (!aligned16(T)) return fail(QGEMM_ERR_ALIGN, "T must be 16-byte aligned");
+        if ((size_t)(K / block) > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "too many blocks per channel");
+        e = qg::launch_quant_pack(W, K, N, block, mode == QGEMM_MODE_INT8 ? 8 : 4, static_cast<uint8_t*>(Bp), T, s);
+    }
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_pack launch");
+}
+
+int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp, const float* T,
+              void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_shape(K, N, mode, &block);
+    if (rc != QGEMM_OK) return rc;
+    if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
+    if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
+        return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (!A || !Bp || !C) return fail(QGEMM_ERR_ARG, "null A, Bp or C");
+    if (mode != QGEMM_MODE_FLOAT && !T) return fail(QGEMM_ERR_ARG, "null T");
+    if (!aligned16(A) || !aligned16(Bp) || !aligned16(C) || (T && !aligned16(T)) ||
+        (workspace && !aligned16(workspace)))
+        return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C and workspace must be 16-byte aligned");
+    if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
+    const size_t need = run_ws(M, K, N, mode, block, a_dtype);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+
+    if (mode == QGEMM_MODE_W4A8) {
+        int8_t* qa = static_cast<int8_t*>(workspace);
+        float* as = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)M * K));
+        int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
+        e = qg::launch_act_quant(M, K, A, a_dtype, qa, as, rs, s);
+        if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+        qg::W4A8Args w{M, K, N, qa, as, rs, Bp, T, nullptr, C, c_dtype};
+        e = qg::launch_w4a8_gemm(w, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
+    }
+
+    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
+    const Path path = choose_path(M, K, N, mode, a_dtype);
+    if (path == PATH_PREFILL) {
+        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C};
+        e = qg::launch_prefill(pa, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
+    }
+    qg::DecodeArgs da{};
+    da.M = M; da.K = K; da.N = N; da.block = block; da.fmt = fmt;
+    da.a_dtype = a_dtype; da.c_dtype = c_dtype;
+    da.A = A; da.Bp = Bp; da.T = T; da.C = C;
+    if (path == PATH_F32) {
+        da.splits = 1;
+        e = qg::launch_decode_f32(da, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode_f32 launch");
+    }
+    da.splits = qg::decode_splits(M, K, N);
+    da.partial = da.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    e = qg::launch_decode(da, s);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode launch");
+}
+
+int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* a_scale, int32_t* rowsum,
+                    void* stream) {
+    if (M < 0 || K <= 0) return fail(QGEMM_ERR_ARG, "invalid sizes M=%d K=%d", M, K);
+    if (K % 64 != 0) return fail(QGEMM_ERR_UNSUPPORTED, "K=%d is not a multiple of 64", K);
+    if (!valid_dtype(a_dtype)) return fail(QGEMM_ERR_ARG, "unknown a_dtype %d", a_dtype);
+    if (M == 0) return QGEMM_OK;
+    if (!A || !qa || !a_scale || !rowsum) return fail(QGEMM_ERR_ARG, "null pointer");
+    if (!aligned16(A) || !aligned16(qa) || !aligned16(a_scale) || !aligned16(rowsum))
+        return fail(QGEMM_ERR_ALIGN, "pointers must be 16-byte aligned");
+    cudaError_t e = qg::launch_act_quant(M, K, A, a_dtype, qa, a_scale, rowsum, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "act_quant launch");
+}
+
+int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* stream) {
+    int block = 0;
+    int rc = check_shape(K, N, QGEMM_MODE_W4A8, &block);
+    if (rc != QGEMM_OK) return rc;
+    if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (!qa || !Bp || !acc) return fail(QGEMM_ERR_ARG, "null pointer");
+    if (!aligned16(qa) || !aligned16(Bp) || !aligned16(acc))
+        return fail(QGEMM_ERR_ALIGN, "pointers must be 16-byte aligned");
+    qg::W4A8Args w{M, K, N, qa, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
+    cudaError_t e = qg::launch_w4a8_gemm(w, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
+}
+
+int qgemm_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int v = 0;
+    e = qg::read_and_clear_status(&v, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (v != 0) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status word 0x%x)", v);
+    return QGEMM_OK;
+}
+
+const char* qgemm_error_string(int code) {
+    switch (code) {
+        case QGEMM_OK: return "QGEMM_OK";
+        case QGEMM_ERR_ARG: return "QGEMM_ERR_ARG";
+        case QGEMM_ERR_UNSUPPORTED: return "QGEMM_ERR_UNSUPPORTED";
+        case QGEMM_ERR_ALIGN: return "QGEMM_ERR_ALIGN";
+        case QGEMM_ERR_WORKSPACE: return "QGEMM_ERR_WORKSPACE";
+        case QGEMM_ERR_CUDA: return "QGEMM_ERR_CUDA";
+        case QGEMM_ERR_TIMEOUT: return "QGEMM_ERR_TIMEOUT";
+        default: return "QGEMM_ERR_UNKNOWN";
+    }
+}
+
+const char* qgemm_last_error(void) { return g_last_error; }
+
+}  // extern "C"
