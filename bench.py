@@ -255,46 +255,57 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
             raise qg.QgemmError(rc, "qgemm_run")
 
     launches_per_call = 1 + (1 if (w.mode == synth.MODE_W4A8) else 0)
-    # warm-up (eager) and graph capture of exactly K calls
+    # warm-up (eager), then one CUDA graph of exactly K calls per launch mode: plain stream
+    # order, and with QGEMM_OPT_LAUNCH_OVERLAP (each decode call may start while the previous
+    # one finishes; it prefetches weights and waits for the previous kernel before A and C).
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             call(i)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(args.steps):
-            call(i)
-    stream.synchronize()
-    graph.replay()          # one untimed replay: the graph's own first-launch cost stays out
+    graphs = {}
+    for mode in (0, 1):
+        qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, mode)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(args.steps):
+                call(i)
+        graphs[mode] = g
+    qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 0)
     stream.synchronize()
 
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(device.index if device.index is not None else 0) as clk:
-        t_wall = time.perf_counter()
+    def timed(g):
+        g.replay()          # one untimed replay: the graph's own first-launch cost stays out
+        stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             start.record(stream)
-            graph.replay()
+            g.replay()
             end.record(stream)
         stream.synchronize()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        ms = start.elapsed_time(end)
+        if dist is not None:
+            t = torch.tensor([ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    ms_plain = timed(graphs[0])
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        t_wall = time.perf_counter()
+        ms = timed(graphs[1])
         t_wall = time.perf_counter() - t_wall
         if t_wall < 1.0:    # keep the sampler running long enough to see the load (replays are identical)
-            reps = int(1.0 / max(t_wall, 1e-4))
             with torch.cuda.stream(stream):
-                for _ in range(min(reps, 2000)):
-                    graph.replay()
+                for _ in range(min(int(1.0 / max(t_wall, 1e-4)), 2000)):
+                    graphs[1].replay()
             stream.synchronize()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     clocks = clk.summary()
 
     # end to end through the public API with host buffers: H2D of A, the call, D2H of C, per step
@@ -311,7 +322,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
             C_host.copy_(C, non_blocking=True)
             stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    return {"ms": ms, "clocks": clocks, "copies": copies, "copy_bytes": copy_bytes, "l2": l2,
+    return {"ms": ms, "ms_plain": ms_plain, "clocks": clocks, "copies": copies, "copy_bytes": copy_bytes, "l2": l2,
             "launches_per_call": launches_per_call, "e2e_s": e2e_s,
             "h2d": A.numel() * A.element_size(), "d2h": C.numel() * C.element_size()}
 
@@ -322,12 +333,16 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.m:
+        import dataclasses
+        w = dataclasses.replace(w, M=args.m)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -376,8 +391,12 @@ def main():
         "config": dict(base_config, parallelism=f"replicas x{world}",
                        l2=f"{r['copies']} rotating weight copies of {r['copy_bytes'] / 1e6:.1f} MB "
                           f"(> 3x the {r['l2'] / 1e6:.0f} MB L2)",
-                       timing=f"CUDA graph of {args.steps} back-to-back calls, CUDA events"),
+                       timing=f"CUDA graph of {args.steps} back-to-back calls, CUDA events",
+                       launch_overlap="QGEMM_OPT_LAUNCH_OVERLAP=1 (programmatic dependent launch)"),
         "tflops": tflops, "gbs": gbs,
+        "ms_per_step_no_overlap": r["ms_plain"] / args.steps,
+        "value_no_overlap": (alg / (r["ms_plain"] / 1e3 / args.steps) / 1e9 * world) if bound == "hbm"
+        else (w.flops / (r["ms_plain"] / 1e3 / args.steps) / 1e12 * world),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "traffic": measured_traffic(w.name), "algorithmic_bytes": alg},

@@ -122,6 +122,23 @@ int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float*
  * 4-bit codes of Bp [N][K/2] read as int8 values 0..15. Writes acc int32 [M][N]. */
 int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* stream);
 
+/* ---------------------------------------------------------------- options */
+
+/* QGEMM_OPT_LAUNCH_OVERLAP (default 0). When 1, the decode kernel (M <= 16) is launched with a
+ * programmatic dependency on the previous kernel in the stream: it may start while that
+ * kernel is finishing, begins streaming Bp and T at once, and waits for the previous kernel
+ * to complete before it reads A or writes C or the workspace. This hides the launch and
+ * weight-fetch latency of back-to-back layer calls. CONTRACT while enabled: the kernel
+ * launched immediately before qgemm_run on the same stream must not write Bp or T.
+ * The setting is process-wide. */
+#define QGEMM_OPT_LAUNCH_OVERLAP 1
+
+/* Set an option; returns its previous value, or QGEMM_ERR_ARG for an unknown option or value. */
+int qgemm_set_option(int option, int value);
+
+/* Current value of an option, or QGEMM_ERR_ARG for an unknown option. */
+int qgemm_get_option(int option);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronize `stream`, then report (and clear) the library's device status word: QGEMM_OK,

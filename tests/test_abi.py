@@ -94,6 +94,16 @@ def test_pack_and_aux_reject():
     assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, None) == -1
 
 
+def test_options():
+    assert qg.qgemm_get_option(qg.OPT_LAUNCH_OVERLAP) == 0
+    assert qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 1) == 0
+    assert qg.qgemm_get_option(qg.OPT_LAUNCH_OVERLAP) == 1
+    assert qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 0) == 1
+    assert qg.load().qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 2) == -1
+    assert qg.load().qgemm_set_option(99, 0) == -1
+    assert qg.load().qgemm_get_option(99) == -1
+
+
 def test_error_strings():
     for code, name in qg.ERRORS.items():
         assert qg.qgemm_error_string(code) == name

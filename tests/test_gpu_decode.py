@@ -173,3 +173,56 @@ def test_act_quant_bit_exact(a_dtype):
     assert np.array_equal(qa.cpu().numpy(), qa_r)
     assert np.array_equal(s.cpu().numpy(), s_r)
     assert np.array_equal(rs.cpu().numpy(), rs_r)
+
+
+def test_launch_overlap_chained_layers_bit_identical():
+    """With QGEMM_OPT_LAUNCH_OVERLAP each decode call may start before the previous kernel ends;
+    it must still read A (here: the previous layer's output) only after that kernel is done.
+    Four chained layers (square, K = N) give identical bits with and without the option."""
+    K = N = 2048
+    layers = []
+    for i in range(4):
+        w = synth.Workload("t", 1, K, N, 1, 64, synth.BF16, synth.BF16, 1, 10 + i, w_std=0.04)
+        layers.append(gpu_pack(synth.make_weights(w), 1, 64))
+    A0 = torch_from(synth.make_activations(synth.Workload("t", 1, K, N, 1, 64, 2, 2, 3, 0)), synth.BF16)
+    wsb = qg.qgemm_workspace_bytes(1, K, N, 1, 64, 2, 2)     # N = 2048 also exercises split-K
+    assert wsb > 0
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+
+    def chain():
+        x = A0
+        outs = []
+        for Bp, T in layers:
+            y = torch.empty((1, N), dtype=torch.bfloat16, device=DEV)
+            qg.qgemm_run(1, K, N, 1, 64, x, 2, Bp, T, y, 2, ws, wsb)
+            outs.append(y)
+            x = y
+        torch.cuda.synchronize()
+        return [o.float().cpu().numpy() for o in outs]
+
+    prev = qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 0)
+    try:
+        ref = chain()
+        qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 1)
+        for _ in range(3):
+            got = chain()
+            for a, b in zip(ref, got):
+                assert np.array_equal(a, b)
+        # inside a CUDA graph as well
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            x = A0
+            outs = []
+            with torch.cuda.graph(g, stream=s):
+                for Bp, T in layers:
+                    y = torch.empty((1, N), dtype=torch.bfloat16, device=DEV)
+                    qg.qgemm_run(1, K, N, 1, 64, x, 2, Bp, T, y, 2, ws, wsb, stream=s)
+                    outs.append(y)
+                    x = y
+        g.replay()
+        torch.cuda.synchronize()
+        for a, o in zip(ref, outs):
+            assert np.array_equal(a, o.float().cpu().numpy())
+    finally:
+        qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, prev)

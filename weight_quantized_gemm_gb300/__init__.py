@@ -15,10 +15,12 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
 MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
+OPT_LAUNCH_OVERLAP = 1
 F32, F16, BF16 = 0, 1, 2
 OK = 0
 ERRORS = {-1: "QGEMM_ERR_ARG", -2: "QGEMM_ERR_UNSUPPORTED", -3: "QGEMM_ERR_ALIGN", -4: "QGEMM_ERR_WORKSPACE",
@@ -38,6 +40,8 @@ SIGNATURES = {
     "qgemm_act_quant": ([_I, _I, _P, _I, _P, _P, _P, _P], _I),
     "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P], _I),
     "qgemm_status": ([_P], _I),
+    "qgemm_set_option": ([_I, _I], _I),
+    "qgemm_get_option": ([_I], _I),
     "qgemm_error_string": ([_I], ctypes.c_char_p),
     "qgemm_last_error": ([], ctypes.c_char_p),
 }
@@ -125,6 +129,20 @@ def qgemm_w4a8_acc(M: int, K: int, N: int, qa, Bp, acc, stream=None) -> None:
 
 def qgemm_status(stream=None) -> int:
     return load().qgemm_status(_stream(stream))
+
+
+def qgemm_set_option(option: int, value: int) -> int:
+    rc = load().qgemm_set_option(option, value)
+    if rc < 0:
+        raise QgemmError(rc, "qgemm_set_option")
+    return rc
+
+
+def qgemm_get_option(option: int) -> int:
+    rc = load().qgemm_get_option(option)
+    if rc < 0:
+        raise QgemmError(rc, "qgemm_get_option")
+    return rc
 
 
 def qgemm_error_string(code: int) -> str:

@@ -34,6 +34,7 @@ struct DecodeArgs {
     void* C;
     float* partial;   // [splits][M][N] f32 partial sums when splits > 1
     int splits;       // number of K-splits across thread blocks (>= 1)
+    int overlap;      // launch with a programmatic dependency on the previous kernel
 };
 // K-splits the decode kernel uses for this shape (1 = none).
 int decode_splits(int M, int K, int N);
@@ -67,6 +68,9 @@ struct W4A8Args {
     int c_dtype;
 };
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
+
+// library options (qgemm_set_option)
+int option_overlap();
 
 // device status word (bounded waits that gave up); read and cleared by qgemm_status
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);

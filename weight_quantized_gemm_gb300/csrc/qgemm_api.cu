@@ -3,12 +3,15 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "../../include/qgemm.h"
 #include "internal.h"
 
 namespace {
 
 thread_local char g_last_error[256] = "";
+std::atomic<int> g_opt_overlap{0};
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -65,14 +68,31 @@ Path choose_path(int M, int K, int N, int mode, int a_dtype) {
 size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype) {
     if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K);
     if (choose_path(M, K, N, mode, a_dtype) != PATH_DECODE) return 0;
-    const int splits = qg::decode_splits(M, K, N);
-    return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    // the decode kernel runs 16 rows of A at a time; split-K partials are per 16-row launch
+    const int mc = M < 16 ? M : 16;
+    const int splits = qg::decode_splits(mc, K, N);
+    return splits > 1 ? (size_t)splits * mc * N * sizeof(float) : 0;
     (void)block;
 }
 
 }  // namespace
 
+int qg::option_overlap() { return g_opt_overlap.load(std::memory_order_relaxed); }
+
 extern "C" {
+
+int qgemm_set_option(int option, int value) {
+    if (option == QGEMM_OPT_LAUNCH_OVERLAP) {
+        if (value != 0 && value != 1) return fail(QGEMM_ERR_ARG, "option %d takes 0 or 1, got %d", option, value);
+        return g_opt_overlap.exchange(value);
+    }
+    return fail(QGEMM_ERR_ARG, "unknown option %d", option);
+}
+
+int qgemm_get_option(int option) {
+    if (option == QGEMM_OPT_LAUNCH_OVERLAP) return g_opt_overlap.load();
+    return fail(QGEMM_ERR_ARG, "unknown option %d", option);
+}
 
 size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype) {
     int block = 0;
@@ -160,8 +180,9 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
         e = qg::launch_decode_f32(da, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode_f32 launch");
     }
-    da.splits = qg::decode_splits(M, K, N);
-    da.partial = da.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    da.splits = 1;   // chosen per 16-row launch inside launch_decode
+    da.overlap = qg::option_overlap();
+    da.partial = static_cast<float*>(workspace);
     e = qg::launch_decode(da, s);
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode launch");
 }
