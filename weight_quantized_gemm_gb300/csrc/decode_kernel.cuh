@@ -43,7 +43,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr size_t kMaxSmem = 232448;   // opt-in shared memory per thread block on sm_100-class GPUs
 // cp.async stages per warp for the Int4 weight stream (build-time tuning constant, 2..5)
 #ifndef QG_DEC_DEPTH_INT4
-#define QG_DEC_DEPTH_INT4 5
+#define QG_DEC_DEPTH_INT4 3
 #endif
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
@@ -114,6 +114,35 @@ __device__ __forceinline__ void int4_pairs(uint32_t w, uint32_t* p) {
     p[1] = lop3_and_or(w >> 4, 0x000F000Fu, kMagic);
     p[2] = lop3_and_or(w >> 8, 0x000F000Fu, kMagic);
     p[3] = lop3_and_or(w >> 12, 0x000F000Fu, kMagic);
+}
+
+// The A operand of MMA q is the quad {row g pair (2q), row g+8 pair (2q), row g pair (2q+1),
+// row g+8 pair (2q+1)}. These helpers write conversions straight into such quads (a[q][0..3])
+// so that no register moves are needed to assemble them.
+template <bool BF>
+__device__ __forceinline__ void int4_to_quads(uint32_t w, uint32_t (*a)[4], int row) {
+    // word u of a row feeds MMAs 2u, 2u + 1; the caller passes a = &quads[2u], row 0 (g) or 1 (g + 8)
+    constexpr uint32_t kMagic = BF ? 0x43004300u : 0x64006400u;
+    a[0][row] = lop3_and_or(w, 0x000F000Fu, kMagic);            // (n0, n4)
+    a[0][row + 2] = lop3_and_or(w >> 4, 0x000F000Fu, kMagic);   // (n1, n5)
+    a[1][row] = lop3_and_or(w >> 8, 0x000F000Fu, kMagic);       // (n2, n6)
+    a[1][row + 2] = lop3_and_or(w >> 12, 0x000F000Fu, kMagic);  // (n3, n7)
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
 }
 
 // 4 bytes b0..b3 -> p[0] = (b0, b1), p[1] = (b2, b3). f16: 1024 + b. bf16: b itself (8-bit
@@ -245,6 +274,93 @@ __device__ __forceinline__ float2 col_sums(const uint32_t* b) {
     return make_float2(d[0], d[1]);
 }
 
+// Everything one warp needs to issue the cp.async copies of one unit into one ring stage. All
+// members are per-warp or per-lane constants, computed once, so issuing a unit costs only the
+// row arithmetic and the copies themselves.
+template <int FMT, int NT, bool PERCH, bool FULL>
+struct Issuer {
+    using R = Ring<FMT, NT, PERCH>;
+    static constexpr int SBW = Share<NT>::kSbw;
+    static constexpr bool kScaled = FMT != FMT_FLOAT && !PERCH;
+    const uint8_t* bp;     // Bp + this lane's byte offset inside a row
+    const float* T;
+    size_t row_bytes;
+    int N, nb, g, lane;
+    int sb0;               // global index of the warp's first sub-block
+    int sb_per_blk;        // sub-blocks per table block
+    unsigned valid;        // bit j: the warp's sub-block j lies inside the K-range
+    bool tab16;            // a pair's two table entries are one aligned 16-byte copy
+    uint32_t wdst0, wdst1; // this lane's weight destinations inside a stage (rows g, g + 8)
+    uint32_t tdst;         // this lane's table destination inside a stage (4-byte copies)
+    int trow;              // the table row this lane copies (4-byte copies)
+
+    __device__ __forceinline__ bool ok(int j) const { return FULL || ((valid >> j) & 1u); }
+    // table column of the warp's sub-block j (j is a compile-time constant after unrolling)
+    __device__ __forceinline__ int blk(int j) const {
+        const int sb = sb0 + sbl_of<FMT>(0, j);
+        return sb_per_blk == 1 ? sb : sb / sb_per_blk;
+    }
+
+    __device__ __forceinline__ void operator()(int n0, uint32_t st) const {
+        const int r0 = min(n0 + g, N - 1), r1 = min(n0 + g + 8, N - 1);
+        const uint8_t* w0 = bp + (size_t)r0 * row_bytes;
+        const uint8_t* w1 = bp + (size_t)r1 * row_bytes;
+        if constexpr (R::kPair) {
+            const int t = lane & 3;
+#pragma unroll
+            for (int jp = 0; jp < R::kGroups; ++jp) {
+                if (!ok(2 * jp)) continue;
+                const uint32_t sg = st + jp * R::kGroupBytes;
+                const size_t o = (size_t)jp * 2 * kWarps * R::kRowBytesPerSb;
+                if (ok(2 * jp + 1) || t < 2) {
+                    cp_async16(sg + wdst0, w0 + o);
+                    cp_async16(sg + wdst1, w1 + o);
+                }
+                if constexpr (kScaled) {
+                    // lanes 16 * q + r copy row r's {offset, scale} pairs of copy group q (all
+                    // lanes copy group 0 when a stage holds one group)
+                    const int q = R::kGroups == 2 ? (lane >> 4) : 0;
+                    if (q == jp) {
+                        const int rr = lane & 15;
+                        const float* src = T + ((size_t)min(n0 + rr, N - 1) * nb + blk(2 * jp)) * 2;
+                        const uint32_t dst = sg + 1024 + rr * 16;
+                        if (tab16 && ok(2 * jp + 1)) {
+                            cp_async16(dst, src);
+                        } else {
+                            cp_async8(dst, src);
+                            if (ok(2 * jp + 1))
+                                cp_async8(dst + 8, src + 2 * (blk(2 * jp + 1) - blk(2 * jp)));
+                        }
+                    }
+                }
+            }
+        } else {
+            const int rt = min(n0 + trow, N - 1);
+#pragma unroll
+            for (int j = 0; j < SBW; ++j) {
+                if (!ok(j)) continue;
+                const uint32_t sj = st + j * R::kGroupBytes;
+                const size_t o = (size_t)j * kWarps * R::kRowBytesPerSb;
+                if constexpr (FMT == FMT_INT8) {
+                    cp_async16(sj + wdst0, w0 + o);
+                    cp_async16(sj + wdst1, w1 + o);
+                } else {
+                    cp_async16(sj + wdst0, w0 + o);
+                    cp_async16(sj + wdst0 + 512, w0 + o + 16);
+                    cp_async16(sj + wdst1, w1 + o);
+                    cp_async16(sj + wdst1 + 512, w1 + o + 16);
+                }
+                if constexpr (kScaled)
+                    cp_async4(sj + 32 * R::kLaneBytes + tdst, T + ((size_t)rt * nb + blk(j)) * 2 + (lane & 1));
+            }
+        }
+        if constexpr (PERCH && FMT != FMT_FLOAT) {
+            const int rt = min(n0 + trow, N - 1);
+            cp_async4(st + R::kGroups * R::kGroupBytes + tdst, T + (size_t)rt * 2 + (lane & 1));
+        }
+    }
+};
+
 // One persistent thread block: units of 16 output channels (blockIdx.x, +gridDim.x, ...) over
 // the K-range of split blockIdx.y, for at most 8 * NT rows of A.
 //   ONECOL: M == 1, so only MMA column 0 carries data and only it is scaled.
@@ -277,93 +393,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
     uint8_t* ring = reinterpret_cast<uint8_t*>(red + 2 * kWarps * NT * 128) + (size_t)warp * D * R::kStageBytes;
     const uint32_t ring_s = smem_u32(ring);
 
-    // this warp's sub-blocks (the same in every unit) and its units
-    bool valid[SBW];
-    int blk[SBW];
+    Issuer<FMT, NT, PERCH, FULL> issue;
+    issue.valid = 0;
 #pragma unroll
-    for (int j = 0; j < SBW; ++j) {
-        valid[j] = FULL || sbl_of<FMT>(warp, j) < nsbc;
-        const int sb = sb_begin + sbl_of<FMT>(warp, j);
-        blk[j] = sb_per_blk == 1 ? sb : sb / sb_per_blk;
+    for (int j = 0; j < SBW; ++j) issue.valid |= (sbl_of<FMT>(warp, j) < nsbc ? 1u : 0u) << j;
+    issue.sb0 = sb_begin + sbl_of<FMT>(warp, 0);
+    issue.sb_per_blk = sb_per_blk;
+    issue.row_bytes = (size_t)nsb * R::kRowBytesPerSb;
+    issue.bp = static_cast<const uint8_t*>(p.Bp) + (size_t)(sb_begin + sbl_of<FMT>(warp, 0)) * R::kRowBytesPerSb +
+               t * (R::kPair ? 16 : R::kRowBytesPerSb / 4);
+    issue.T = p.T;
+    issue.N = N;
+    issue.nb = nb;
+    issue.g = g;
+    issue.lane = lane;
+    issue.tab16 = sb_per_blk == 1 && (nb & 1) == 0 && (sb_begin & 1) == 0;
+    if constexpr (R::kPair) {
+        issue.wdst0 = (uint32_t)(g * 64 + ((t ^ (g & 3)) << 4));
+        issue.wdst1 = issue.wdst0 + 512;
+    } else {
+        issue.wdst0 = (uint32_t)(lane * 16);
+        issue.wdst1 = issue.wdst0 + (FMT == FMT_INT8 ? 512 : 1024);
     }
-    const int nu = (int)blockIdx.x < groups ? (groups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-    const uint8_t* Bp = static_cast<const uint8_t*>(p.Bp);
-    const size_t row_bytes = (size_t)nsb * R::kRowBytesPerSb;
-    const size_t lane_off = (size_t)(sb_begin + sbl_of<FMT>(warp, 0)) * R::kRowBytesPerSb +
-                            t * (R::kPair ? 16 : R::kRowBytesPerSb / 4);
-    // the table word this lane copies: slot s = lane >> 1 holds row (s >> 1) + 8 * (s & 1), word lane & 1
-    const int trow = (lane >> 2) + 8 * ((lane >> 1) & 1);
-    const uint32_t tdst = (uint32_t)((lane >> 1) * 8 + (lane & 1) * 4);
+    // slot s = lane >> 1 holds row (s >> 1) + 8 * (s & 1), word lane & 1
+    issue.trow = (lane >> 2) + 8 * ((lane >> 1) & 1);
+    issue.tdst = (uint32_t)((lane >> 1) * 8 + (lane & 1) * 4);
 
-    auto issue = [&](int ui) {
-        if (ui < nu) {
-            const int n0 = ((int)blockIdx.x + ui * (int)gridDim.x) * 16;
-            const int r0 = min(n0 + g, N - 1), r1 = min(n0 + g + 8, N - 1);
-            const int rt = min(n0 + trow, N - 1);
-            const uint8_t* w0 = Bp + (size_t)r0 * row_bytes + lane_off;
-            const uint8_t* w1 = Bp + (size_t)r1 * row_bytes + lane_off;
-            const uint32_t st = ring_s + (uint32_t)((ui % D) * R::kStageBytes);
-            if constexpr (R::kPair) {
-                const uint32_t swz = (uint32_t)((t ^ (g & 3)) << 4);
-#pragma unroll
-                for (int jp = 0; jp < R::kGroups; ++jp) {
-                    if (!valid[2 * jp]) continue;
-                    const uint32_t sg = st + jp * R::kGroupBytes;
-                    const size_t o = (size_t)jp * 2 * kWarps * R::kRowBytesPerSb;
-                    if (FULL || valid[2 * jp + 1] || t < 2) {
-                        cp_async16(sg + g * 64 + swz, w0 + o);
-                        cp_async16(sg + (g + 8) * 64 + swz, w1 + o);
-                    }
-                    if constexpr (kScaled) {
-                        // lanes 16 * q + r copy row r's {offset, scale} of copy group q (all lanes
-                        // of group 0 when a stage holds one group)
-                        const int q = R::kGroups == 2 ? (lane >> 4) : 0;
-                        if (q == jp) {
-                            const int rr = lane & 15;
-                            const int ch = min(n0 + rr, N - 1);
-                            const uint32_t dst = sg + 1024 + rr * 16;
-                            if (sb_per_blk == 1 && (FULL || valid[2 * jp + 1])) {
-                                cp_async16(dst, p.T + ((size_t)ch * nb + blk[2 * jp]) * 2);
-                            } else {
-                                cp_async8(dst, p.T + ((size_t)ch * nb + blk[2 * jp]) * 2);
-                                if (FULL || valid[2 * jp + 1])
-                                    cp_async8(dst + 8, p.T + ((size_t)ch * nb + blk[2 * jp + 1]) * 2);
-                            }
-                        }
-                    }
-                }
-            } else {
-#pragma unroll
-            for (int j = 0; j < SBW; ++j) {
-                if (!valid[j]) continue;
-                const uint32_t sj = st + j * R::kGroupBytes;
-                const size_t o = (size_t)j * kWarps * R::kRowBytesPerSb;
-                if constexpr (FMT == FMT_INT8) {
-                    cp_async16(sj + lane * 16, w0 + o);
-                    cp_async16(sj + 512 + lane * 16, w1 + o);
-                } else {
-                    cp_async16(sj + lane * 16, w0 + o);
-                    cp_async16(sj + 512 + lane * 16, w0 + o + 16);
-                    cp_async16(sj + 1024 + lane * 16, w1 + o);
-                    cp_async16(sj + 1536 + lane * 16, w1 + o + 16);
-                }
-                if constexpr (kScaled)
-                    cp_async4(sj + 32 * R::kLaneBytes + tdst, p.T + ((size_t)rt * nb + blk[j]) * 2 + (lane & 1));
-            }
-            }
-            if constexpr (PERCH && FMT != FMT_FLOAT)
-                cp_async4(st + R::kGroups * R::kGroupBytes + tdst, p.T + (size_t)rt * 2 + (lane & 1));
-        }
-        cp_async_commit();
-    };
+    const int nu = (int)blockIdx.x < groups ? (groups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    const int n_step = (int)gridDim.x * 16;
 
     // Let the next kernel on the stream launch (it only takes SMs as these blocks exit), start
     // the weight stream, then wait for the previous kernel's results before touching A or C.
     // Both griddepcontrol instructions are no-ops unless the launch carried the programmatic
     // serialization attribute.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int issue_ui = 0;
+    uint32_t issue_st = ring_s;
 #pragma unroll
-    for (int i = 0; i < D - 1; ++i) issue(i);
+    for (int i = 0; i < D - 1; ++i) {
+        if (issue_ui < nu) issue((int)blockIdx.x * 16 + issue_ui * n_step, issue_st);
+        cp_async_commit();
+        ++issue_ui;
+        issue_st = (i + 1 == D) ? ring_s : issue_st + R::kStageBytes;
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const uint16_t* A = static_cast<const uint16_t*>(p.A);
@@ -377,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
         for (int j = 0; j < SBW; ++j) {
 #pragma unroll
             for (int q = 0; q < 8; ++q) nw[j][q] = 0u;
-            if (valid[j] && g < M) {
+            if (issue.ok(j) && g < M) {
                 const uint4* src = reinterpret_cast<const uint4*>(
                     A + (size_t)g * K + (size_t)(sb_begin + sbl_of<FMT>(warp, j)) * 64 + t * 16);
                 const uint4 x = src[0], y = src[1];
@@ -389,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
         for (int j = 0; j < SBW; ++j) {
             b_frags<FMT>(nw[j], breg[j]);
             sreg[j] = col_sums<BF>(breg[j]);
-            if (valid[j] && g == 0) {
+            if (issue.ok(j) && g == 0) {
                 asum[sbl_of<FMT>(warp, j) * 8 + 2 * t] = sreg[j].x;
                 asum[sbl_of<FMT>(warp, j) * 8 + 2 * t + 1] = sreg[j].y;
             }
@@ -427,62 +499,83 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
         __syncthreads();
     }
 
+    // per-lane read offsets inside a stage
+    int roff0 = 0, roff1 = 0, toff = 0;
+    if constexpr (R::kPair) {
+        roff0 = g * 64 + ((((t >> 1)) ^ (g & 3)) << 4) + ((t & 1) << 3);       // sub-block 0 of a pair
+        roff1 = g * 64 + ((((2 + (t >> 1))) ^ (g & 3)) << 4) + ((t & 1) << 3); // sub-block 1 of a pair
+        toff = 1024 + g * 16;
+    } else {
+        roff0 = lane * 16;
+        toff = 32 * R::kLaneBytes + g * 16;
+    }
+
     float acc[NT][4], dp[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[nt][c] = dp[nt][c] = 0.f;
 
+    uint32_t cons = ring_s;   // stage being consumed (shared-space address)
     for (int ui = 0; ui < nu; ++ui) {
-        const int n0 = ((int)blockIdx.x + ui * (int)gridDim.x) * 16;
-        issue(ui + D - 1);
+        const int n0 = (int)blockIdx.x * 16 + ui * n_step;
+        if (issue_ui < nu) issue((int)blockIdx.x * 16 + issue_ui * n_step, issue_st);
+        cp_async_commit();
+        ++issue_ui;
+        issue_st = (issue_st + R::kStageBytes == ring_s + D * R::kStageBytes) ? ring_s : issue_st + R::kStageBytes;
         cp_async_wait<D - 1>();
         __syncwarp();
-        const uint8_t* st = ring + (size_t)(ui % D) * R::kStageBytes;
+        const uint32_t st = cons;
+        cons = (cons + R::kStageBytes == ring_s + D * R::kStageBytes) ? ring_s : cons + R::kStageBytes;
         float4 tcc = make_float4(0.f, 0.f, 0.f, 0.f);   // per-channel {o_g, s_g, o_g+8, s_g+8}
-        if constexpr (PERCH && FMT != FMT_FLOAT)
-            tcc = reinterpret_cast<const float4*>(st + R::kGroups * R::kGroupBytes)[g];
+        if constexpr (PERCH && FMT != FMT_FLOAT) tcc = lds128f(st + R::kGroups * R::kGroupBytes + g * 16);
+        float4 tpair0 = make_float4(0.f, 0.f, 0.f, 0.f), tpair1 = tpair0;   // Int4: the current pair's table
 #pragma unroll
         for (int j = 0; j < SBW; ++j) {
-            if (!valid[j]) continue;
-            // A operand for MMA i: (fa0[2i], fa1[2i], fa0[2i+1], fa1[2i+1]); fa0 = channel row g, fa1 = g + 8
-            uint32_t fa0[8], fa1[8];
+            if (!issue.ok(j)) continue;
+            uint32_t a[4][4];   // A operand quads of the sub-block's 4 MMAs
             float s0 = 0.f, o0 = 0.f, s1 = 0.f, o1 = 0.f;
             if constexpr (FMT == FMT_INT4) {
-                const uint8_t* sg = st + (j >> 1) * R::kGroupBytes;
-                const int off = ((((2 * (j & 1)) + (t >> 1)) ^ (g & 3)) << 4) + ((t & 1) << 3);
-                const uint2 x0 = *reinterpret_cast<const uint2*>(sg + g * 64 + off);
-                const uint2 x1 = *reinterpret_cast<const uint2*>(sg + (g + 8) * 64 + off);
-                int4_pairs<BF>(x0.x, fa0);
-                int4_pairs<BF>(x0.y, fa0 + 4);
-                int4_pairs<BF>(x1.x, fa1);
-                int4_pairs<BF>(x1.y, fa1 + 4);
+                const uint32_t sg = st + (j >> 1) * R::kGroupBytes;
+                const uint32_t off = (j & 1) ? (uint32_t)roff1 : (uint32_t)roff0;
+                const uint2 x0 = lds64(sg + off);         // row g: 16 nibbles
+                const uint2 x1 = lds64(sg + off + 512);   // row g + 8
+                int4_to_quads<BF>(x0.x, &a[0], 0);
+                int4_to_quads<BF>(x0.y, &a[2], 0);
+                int4_to_quads<BF>(x1.x, &a[0], 1);
+                int4_to_quads<BF>(x1.y, &a[2], 1);
                 if constexpr (kScaled) {
-                    const float4 ta = reinterpret_cast<const float4*>(sg + 1024)[g];
-                    const float4 tb = reinterpret_cast<const float4*>(sg + 1024)[g + 8];
-                    const float oa = (j & 1) ? ta.z : ta.x, sa = (j & 1) ? ta.w : ta.y;
-                    const float ob = (j & 1) ? tb.z : tb.x, sbv = (j & 1) ? tb.w : tb.y;
+                    if ((j & 1) == 0) {
+                        tpair0 = lds128f(sg + toff);
+                        tpair1 = lds128f(sg + toff + 128);
+                    }
+                    const float oa = (j & 1) ? tpair0.z : tpair0.x, sa = (j & 1) ? tpair0.w : tpair0.y;
+                    const float ob = (j & 1) ? tpair1.z : tpair1.x, sbv = (j & 1) ? tpair1.w : tpair1.y;
                     s0 = sa; o0 = fmaf(-kBias, sa, oa);
                     s1 = sbv; o1 = fmaf(-kBias, sbv, ob);
                 }
             } else {
-                const uint8_t* sj = st + j * R::kGroupBytes;
-                const uint4* planes = reinterpret_cast<const uint4*>(sj);
+                const uint32_t sj = st + j * R::kGroupBytes;
                 if constexpr (FMT == FMT_INT8) {
-                    const uint4 x = planes[lane], y = planes[32 + lane];
-                    int8_pairs<BF>(x.x, fa0); int8_pairs<BF>(x.y, fa0 + 2);
-                    int8_pairs<BF>(x.z, fa0 + 4); int8_pairs<BF>(x.w, fa0 + 6);
-                    int8_pairs<BF>(y.x, fa1); int8_pairs<BF>(y.y, fa1 + 2);
-                    int8_pairs<BF>(y.z, fa1 + 4); int8_pairs<BF>(y.w, fa1 + 6);
+                    const uint4 x = lds128(sj + roff0);         // row g: 16 bytes
+                    const uint4 y = lds128(sj + roff0 + 512);   // row g + 8
+                    const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {   // word q of a row holds MMA q's pairs
+                        uint32_t pr[2];
+                        int8_pairs<BF>(xw[q], pr); a[q][0] = pr[0]; a[q][2] = pr[1];
+                        int8_pairs<BF>(yw[q], pr); a[q][1] = pr[0]; a[q][3] = pr[1];
+                    }
                 } else {
-                    const uint4 x0 = planes[lane], x1 = planes[32 + lane], y0 = planes[64 + lane], y1 = planes[96 + lane];
-                    fa0[0] = x0.x; fa0[1] = x0.y; fa0[2] = x0.z; fa0[3] = x0.w;
-                    fa0[4] = x1.x; fa0[5] = x1.y; fa0[6] = x1.z; fa0[7] = x1.w;
-                    fa1[0] = y0.x; fa1[1] = y0.y; fa1[2] = y0.z; fa1[3] = y0.w;
-                    fa1[4] = y1.x; fa1[5] = y1.y; fa1[6] = y1.z; fa1[7] = y1.w;
+                    const uint4 x0 = lds128(sj + roff0), x1 = lds128(sj + roff0 + 512);
+                    const uint4 y0 = lds128(sj + roff0 + 1024), y1 = lds128(sj + roff0 + 1536);
+                    a[0][0] = x0.x; a[0][2] = x0.y; a[1][0] = x0.z; a[1][2] = x0.w;
+                    a[2][0] = x1.x; a[2][2] = x1.y; a[3][0] = x1.z; a[3][2] = x1.w;
+                    a[0][1] = y0.x; a[0][3] = y0.y; a[1][1] = y0.z; a[1][3] = y0.w;
+                    a[2][1] = y1.x; a[2][3] = y1.y; a[3][1] = y1.z; a[3][3] = y1.w;
                 }
                 if constexpr (kScaled) {
-                    const float4 tt4 = reinterpret_cast<const float4*>(sj + 32 * R::kLaneBytes)[g];
+                    const float4 tt4 = lds128f(sj + toff);
                     s0 = tt4.y; o0 = fmaf(-kBias, tt4.y, tt4.x);
                     s1 = tt4.w; o1 = fmaf(-kBias, tt4.w, tt4.z);
                 }
@@ -505,14 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     if constexpr (FMT == FMT_FLOAT) {
-                        mma16816<BF>(acc[nt], fa0[2 * q], fa1[2 * q], fa0[2 * q + 1], fa1[2 * q + 1], b[2 * q], b[2 * q + 1]);
+                        mma16816<BF>(acc[nt], a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
                     } else if constexpr (kScaled) {
                         if (q == 0)
-                            mma16816_zc<BF>(dp[nt], fa0[0], fa1[0], fa0[1], fa1[1], b[0], b[1]);
+                            mma16816_zc<BF>(dp[nt], a[0][0], a[0][1], a[0][2], a[0][3], b[0], b[1]);
                         else
-                            mma16816<BF>(dp[nt], fa0[2 * q], fa1[2 * q], fa0[2 * q + 1], fa1[2 * q + 1], b[2 * q], b[2 * q + 1]);
+                            mma16816<BF>(dp[nt], a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
                     } else {
-                        mma16816<BF>(dp[nt], fa0[2 * q], fa1[2 * q], fa0[2 * q + 1], fa1[2 * q + 1], b[2 * q], b[2 * q + 1]);
+                        mma16816<BF>(dp[nt], a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
                     }
                 }
                 if constexpr (kScaled) {
@@ -579,7 +672,8 @@ inline int sm_count() {
     static int count = 0;
     if (count == 0) {
         int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             count = kTargetSms;
     }
     return count;
