@@ -327,6 +327,29 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
             "h2d": A.numel() * A.element_size(), "d2h": C.numel() * C.element_size()}
 
 
+def profile_calls(w: synth.Workload, calls: int) -> dict:
+    """Pack the workload's weights and run `calls` plain (eager, non-overlapped) layer calls."""
+    import torch
+
+    import weight_quantized_gemm_gb300 as qg
+    device = torch.device("cuda", torch.cuda.current_device())
+    A = to_torch(synth.make_activations(w), w.a_dtype, device)
+    Wd = torch.from_numpy(synth.make_weights(w)).to(device)
+    pb = qg.qgemm_packed_bytes(w.K, w.N, w.mode, w.a_dtype if w.mode == 0 else 0)
+    tb = qg.qgemm_table_bytes(w.K, w.N, w.mode, w.block)
+    Bp = torch.empty(pb, dtype=torch.uint8, device=device)
+    T = torch.empty(max(tb // 4, 4), dtype=torch.float32, device=device)
+    qg.qgemm_pack(Wd, w.K, w.N, w.mode, w.block, w.a_dtype if w.mode == 0 else 0, Bp, T if tb else None)
+    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
+    C = torch.empty((w.M, w.N), dtype=tdt[w.c_dtype], device=device)
+    wsb = qg.qgemm_workspace_bytes(w.M, w.K, w.N, w.mode, w.block, w.a_dtype, w.c_dtype)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+    for _ in range(calls):
+        qg.qgemm_run(w.M, w.K, w.N, w.mode, w.block, A, w.a_dtype, Bp, T if tb else None, C, w.c_dtype, ws, wsb)
+    torch.cuda.synchronize()
+    return {"workload": w.name, "M": w.M, "calls": calls, "status": qg.qgemm_status()}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -336,6 +359,9 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="pack, run this many plain calls of the layer, print a status line and exit "
+                         "(a small fixed command to run under a profiler; no timing)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -366,6 +392,9 @@ def main():
         return
 
     import torch
+    if args.profile_calls:
+        print(json.dumps(profile_calls(w, args.profile_calls)))
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist_mod

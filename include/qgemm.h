@@ -80,7 +80,7 @@ size_t qgemm_table_bytes(int K, int N, int mode, int block);
 
 /* Bytes of scratch device memory qgemm_run needs for this call (0 if none). The decode
  * path needs it only when it splits K across thread blocks (small N); W4A8 needs it for the
- * quantized activations (M*K bytes of codes, M scales and M row sums). */
+ * quantized activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums). */
 size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype);
 
 /* ---------------------------------------------------------------- weight preparation */
@@ -119,8 +119,14 @@ int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float*
                     void* stream);
 
 /* The W4A8 integer GEMM alone ("S8×S8→S32"): acc[m][n] = sum_k qa[m][k] * q[n][k] with q the
- * 4-bit codes of Bp [N][K/2] read as int8 values 0..15. Writes acc int32 [M][N]. */
-int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* stream);
+ * 4-bit codes of Bp [N][K/2] read as int8 values 0..15. Writes acc int32 [M][N]. The sums are
+ * exact (every partial sum is an integer below 2^24 for K <= 8808). Needs a workspace of
+ * qgemm_w4a8_acc_workspace_bytes(M, K) bytes (the codes as 16-bit operands). */
+int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Workspace bytes qgemm_w4a8_acc needs (0 for invalid sizes). */
+size_t qgemm_w4a8_acc_workspace_bytes(int M, int K);
 
 /* ---------------------------------------------------------------- options */
 

@@ -38,7 +38,8 @@ def test_sizes():
     assert qg.qgemm_packed_bytes(100, 512, qg.MODE_INT4) == 0           # K % 64 != 0
     assert qg.qgemm_table_bytes(256, 512, qg.MODE_INT4, 96) == 0       # block not a multiple of 64
     # W4A8: qa (M*K bytes), scales and row sums, each 256-byte aligned
-    assert qg.qgemm_workspace_bytes(2048, 4096, 14336, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == 2048 * 4096 + 2 * 8192
+    assert qg.qgemm_workspace_bytes(2048, 4096, 14336, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == 2 * 2048 * 4096 + 2 * 8192
+    assert qg.qgemm_w4a8_acc_workspace_bytes(2048, 4096) == 2 * 2048 * 4096
     # decode with a large N needs no scratch; a small N splits K across blocks
     assert qg.qgemm_workspace_bytes(1, 4096, 11008, qg.MODE_INT4, 64, qg.BF16, qg.BF16) == 0
     assert qg.qgemm_workspace_bytes(1, 4096, 512, qg.MODE_INT4, 64, qg.BF16, qg.BF16) > 0
@@ -91,7 +92,8 @@ def test_pack_and_aux_reject():
     assert lib.qgemm_pack(FAKE, 4096, 64, 3, 64, 0, FAKE, FAKE, None) == -2          # W4A8 per channel
     assert lib.qgemm_act_quant(4, 100, FAKE, 2, FAKE, FAKE, FAKE, None) == -2
     assert lib.qgemm_act_quant(4, 128, FAKE, 2, FAKE + 2, FAKE, FAKE, None) == -3
-    assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, None) == -1
+    assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, FAKE, 1 << 20, None) == -1
+    assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, FAKE, FAKE, FAKE, 16, None) == -4      # workspace too small
 
 
 def test_options():

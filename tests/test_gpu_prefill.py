@@ -1,0 +1,144 @@
+"""GPU parity of the tensor-core (tcgen05) path against the CPU oracle, through the C ABI:
+prefill for M > 16 with 16-bit activations in every weight format, and W4A8 (int32
+accumulators bit-exact, rescaled output within the bar)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_quantized_gemm_gb300 as qg
+from weight_quantized_gemm_gb300 import synth
+from tests._util import check_close, ensure_built, to_numpy_values, torch_dtype, torch_from
+from tests.test_gpu_decode import gpu_pack, gpu_run, layer_case
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ensure_built()
+
+
+# ---------------------------------------------------------------- prefill
+@pytest.mark.parametrize("mode,block", [(1, 64), (1, 128), (2, 0), (2, 64), (0, 0)])
+@pytest.mark.parametrize("a_dtype", [synth.F16, synth.BF16])
+@pytest.mark.parametrize("M,K,N", [(17, 64, 1), (64, 256, 128), (100, 512, 257), (256, 192, 130), (300, 1024, 96)])
+def test_prefill_parity(mode, block, a_dtype, M, K, N):
+    if block and K % block:
+        pytest.skip("block does not divide K")
+    layer_case(M, K, N, mode, block, a_dtype, a_dtype)
+
+
+@pytest.mark.parametrize("c_dtype", [synth.F32, synth.F16, synth.BF16])
+def test_prefill_output_dtypes(c_dtype):
+    layer_case(130, 512, 200, 1, 64, synth.F16, c_dtype)
+
+
+def _sampled_case(w: synth.Workload, npts: int = 4096, seed: int = 0):
+    """Full-size layer on the GPU, checked at sampled (m, n) points against the oracle."""
+    A_np = synth.make_activations(w)
+    W_np = synth.make_weights(w)
+    blk = w.K if w.block == 0 else w.block
+    q, T = oracle.quantize(W_np, blk, oracle.QMAX[w.mode])
+    Bp, Tg = gpu_pack(W_np, w.mode, w.block)
+    assert np.array_equal(Bp.cpu().numpy().reshape(w.N, -1), oracle.pack(q, oracle.NBITS[w.mode]))
+    assert np.array_equal(Tg.cpu().numpy().reshape(T.shape), T)
+    got = gpu_run(w.M, w.K, w.N, w.mode, w.block, A_np, w.a_dtype, Bp, Tg, w.c_dtype)
+    rng = np.random.default_rng(seed)
+    mi = rng.integers(0, w.M, npts)
+    ni = rng.integers(0, w.N, npts)
+    mi[:4] = [0, w.M - 1, 0, w.M - 1]
+    ni[:4] = [0, w.N - 1, w.N - 1, 0]
+    R = oracle.gemm_points(oracle.values(A_np, w.a_dtype), q, T, blk, mi, ni)
+    return check_close(got[mi, ni], R, w.a_dtype, w.c_dtype, w.name)
+
+
+def test_int4_b64_prefill_m1024_k4096_n4096():
+    _sampled_case(synth.WORKLOADS["int4_b64_prefill_m1024_k4096_n4096"])
+
+
+def test_float_f16_gemm_full_size_sampled():
+    w = synth.WORKLOADS["float_f16_m2048_k4096_n14336"]
+    A_np = synth.make_activations(w)
+    W_np = synth.make_weights(w)
+    Bp, _ = gpu_pack(W_np, 0, 0, synth.F16)
+    got = gpu_run(w.M, w.K, w.N, 0, 0, A_np, w.a_dtype, Bp, None, w.c_dtype)
+    Wt = oracle.pack_float(W_np, synth.F16)
+    assert np.array_equal(Bp.cpu().numpy().view(np.float16).reshape(w.N, w.K), Wt)
+    rng = np.random.default_rng(1)
+    mi, ni = rng.integers(0, w.M, 2048), rng.integers(0, w.N, 2048)
+    R = oracle.dense_points(oracle.values(A_np, w.a_dtype), oracle.values(Wt, synth.F16), mi, ni)
+    check_close(got[mi, ni], R, w.a_dtype, w.c_dtype, w.name)
+
+
+# ---------------------------------------------------------------- W4A8
+def _w4a8_inputs(M, K, N, a_dtype=synth.BF16, seed=0):
+    w = synth.Workload("t", M, K, N, synth.MODE_W4A8, 0, a_dtype, synth.BF16, seed, seed + 1)
+    return w, synth.make_activations(w), synth.make_weights(w)
+
+
+def _gpu_w4a8_acc(qa_np, Bp, M, K, N):
+    qa = torch.from_numpy(qa_np).to(DEV)
+    acc = torch.full((M, N), -7, dtype=torch.int32, device=DEV)
+    wsb = qg.qgemm_w4a8_acc_workspace_bytes(M, K)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    qg.qgemm_w4a8_acc(M, K, N, qa, Bp, acc, ws, wsb)
+    assert qg.qgemm_status() == 0
+    return acc.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 64, 8), (17, 256, 33), (200, 1024, 300), (64, 4096, 128)])
+def test_w4a8_acc_bit_exact(M, K, N):
+    w, A_np, W_np = _w4a8_inputs(M, K, N)
+    q, T = oracle.quantize(W_np, K, 15)
+    qa, s, rs = oracle.act_quant(oracle.values(A_np, w.a_dtype).astype(np.float32))
+    Bp, _ = gpu_pack(W_np, 3, 0)
+    acc = _gpu_w4a8_acc(qa, Bp, M, K, N)
+    assert np.array_equal(acc, oracle.w4a8_acc(qa, q))
+
+
+def test_w4a8_acc_extreme_codes_exact():
+    """Largest magnitudes the format allows: |qa| = 127 and q = 15 on every k (acc = +-127*15*K)."""
+    M, K, N = 4, 4096, 16
+    qa = np.full((M, K), 127, dtype=np.int8)
+    qa[1] = -127
+    qa[2, ::2] = -127
+    qa[3] = np.where(np.arange(K) % 3 == 0, 127, -1).astype(np.int8)
+    W = np.zeros((K, N), dtype=np.float32)
+    W[0, :] = -1.0
+    W[1:, :] = 1.0                               # codes: 0 at k = 0, 15 elsewhere
+    q, _ = oracle.quantize(W, K, 15)
+    Bp, _ = gpu_pack(W, 3, 0)
+    acc = _gpu_w4a8_acc(qa, Bp, M, K, N)
+    assert np.array_equal(acc, oracle.w4a8_acc(qa, q))
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 128, 40), (33, 512, 100), (300, 1024, 257)])
+@pytest.mark.parametrize("a_dtype", [synth.BF16, synth.F16, synth.F32])
+def test_w4a8_layer(M, K, N, a_dtype):
+    w, A_np, W_np = _w4a8_inputs(M, K, N, a_dtype)
+    ref = oracle.reference_layer(3, 0, A_np, a_dtype, W_np)
+    Bp, T = gpu_pack(W_np, 3, 0)
+    got = gpu_run(M, K, N, 3, 0, A_np, a_dtype, Bp, T, synth.BF16)
+    check_close(got, ref["R"], a_dtype if a_dtype != synth.F32 else synth.BF16, synth.BF16, "w4a8")
+
+
+def test_w4a8_m2048_k4096_n14336_sampled():
+    w = synth.WORKLOADS["w4a8_m2048_k4096_n14336"]
+    A_np = synth.make_activations(w)
+    W_np = synth.make_weights(w)
+    q, T = oracle.quantize(W_np, w.K, 15)
+    qa, s, rs = oracle.act_quant(oracle.values(A_np, w.a_dtype).astype(np.float32))
+    Bp, Tg = gpu_pack(W_np, 3, 0)
+    # int32 accumulators: bit-exact at sampled points
+    acc = _gpu_w4a8_acc(qa, Bp, w.M, w.K, w.N)
+    rng = np.random.default_rng(2)
+    mi, ni = rng.integers(0, w.M, 4096), rng.integers(0, w.N, 4096)
+    acc_ref = oracle.w4a8_acc_points(qa, q, mi, ni)
+    assert np.array_equal(acc[mi, ni], acc_ref)
+    # the layer: within the bar at the same points (expected values from the oracle alone)
+    got = gpu_run(w.M, w.K, w.N, 3, 0, A_np, w.a_dtype, Bp, Tg, w.c_dtype)
+    R = (s[mi].astype(np.float64) * (T[ni, 0, 1].astype(np.float64) * acc_ref.astype(np.float64) +
+                                      T[ni, 0, 0].astype(np.float64) * rs[mi]))
+    check_close(got[mi, ni], R, w.a_dtype, w.c_dtype, w.name)

@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
-    "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
+    "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
     "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
@@ -38,7 +38,8 @@ SIGNATURES = {
     "qgemm_pack": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "qgemm_run": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _SZ, _P], _I),
     "qgemm_act_quant": ([_I, _I, _P, _I, _P, _P, _P, _P], _I),
-    "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P], _I),
+    "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
+    "qgemm_w4a8_acc_workspace_bytes": ([_I, _I], _SZ),
     "qgemm_status": ([_P], _I),
     "qgemm_set_option": ([_I, _I], _I),
     "qgemm_get_option": ([_I], _I),
@@ -123,8 +124,16 @@ def qgemm_act_quant(M: int, K: int, A, a_dtype: int, qa, a_scale, rowsum, stream
            "qgemm_act_quant")
 
 
-def qgemm_w4a8_acc(M: int, K: int, N: int, qa, Bp, acc, stream=None) -> None:
-    _check(load().qgemm_w4a8_acc(M, K, N, _ptr(qa), _ptr(Bp), _ptr(acc), _stream(stream)), "qgemm_w4a8_acc")
+def qgemm_w4a8_acc_workspace_bytes(M: int, K: int) -> int:
+    return load().qgemm_w4a8_acc_workspace_bytes(M, K)
+
+
+def qgemm_w4a8_acc(M: int, K: int, N: int, qa, Bp, acc, workspace=None, workspace_bytes: int | None = None,
+                   stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().qgemm_w4a8_acc(M, K, N, _ptr(qa), _ptr(Bp), _ptr(acc), _ptr(workspace), workspace_bytes,
+                                 _stream(stream)), "qgemm_w4a8_acc")
 
 
 def qgemm_status(stream=None) -> int:

@@ -39,8 +39,8 @@ __device__ __forceinline__ void load8(const void* A, size_t i, float (&v)[8]) {
 
 template <int ADT>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* __restrict__ A,
-                                                             int8_t* __restrict__ qa, float* __restrict__ as,
-                                                             int32_t* __restrict__ rowsum) {
+                                                             int8_t* __restrict__ qa, __half* __restrict__ qa16,
+                                                             float* __restrict__ as, int32_t* __restrict__ rowsum) {
     __shared__ float s_max[kThreads / 32];
     __shared__ int s_sum[kThreads / 32];
     const int m = blockIdx.x;
@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
         float v[8];
         load8<ADT>(A, row + k, v);
         uint32_t packed[2] = {0u, 0u};
+        __half h[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             int c = 0;
@@ -77,8 +78,10 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
             }
             sum += c;
             packed[j >> 2] |= (uint32_t)(c & 0xFF) << (8 * (j & 3));
+            h[j] = __int2half_rn(c);   // |c| <= 127: exact
         }
-        *reinterpret_cast<uint2*>(qa + row + k) = make_uint2(packed[0], packed[1]);
+        if (qa) *reinterpret_cast<uint2*>(qa + row + k) = make_uint2(packed[0], packed[1]);
+        if (qa16) *reinterpret_cast<uint4*>(qa16 + row + k) = *reinterpret_cast<const uint4*>(h);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
@@ -95,14 +98,15 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
 
 }  // namespace
 
-cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* as, int32_t* rowsum,
-                             cudaStream_t s) {
+cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
+                             int32_t* rowsum, cudaStream_t s) {
+    __half* h = static_cast<__half*>(qa16);
     if (a_dtype == DT_F32)
-        act_quant_kernel<DT_F32><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+        act_quant_kernel<DT_F32><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
     else if (a_dtype == DT_F16)
-        act_quant_kernel<DT_F16><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+        act_quant_kernel<DT_F16><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
     else
-        act_quant_kernel<DT_BF16><<<M, kThreads, 0, s>>>(K, A, qa, as, rowsum);
+        act_quant_kernel<DT_BF16><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
     return cudaGetLastError();
 }
 

@@ -53,12 +53,15 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 bool prefill_supported(int M, int K, int N, int fmt, int a_dtype);
 
-cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* as, int32_t* rowsum,
-                             cudaStream_t s);
+// Per-row activation codes: qa (int8) and/or qa16 (the same codes as exact f16 values; either
+// may be null), the row scales and the row sums of the codes.
+cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
+                             int32_t* rowsum, cudaStream_t s);
+cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s);
 // acc (int32 [M][N]) = qa x q^T; or, when acc == nullptr, the rescaled output into C.
 struct W4A8Args {
     int M, K, N;
-    const int8_t* qa;
+    const void* qa16;    // activation codes as f16 [M][K]
     const float* as;
     const int32_t* rowsum;
     const void* Bp;

@@ -1,11 +1,463 @@
-// Tensor-core (tcgen05 / TMEM / TMA) kernels for large M and for W4A8, and the device status
-// word that bounded waits report into.
+// Tensor-core path for larger M (prefill) and for W4A8: tcgen05 MMA with TMEM accumulators.
+//
+// The layer C[M,N] = A[M,K] x dequant(B[K,N]) (benchmark page "MNN GemmSpeed 基准测试实战",
+// «为什么用 Conv1x1 来测 GEMM») is computed transposed, D[n][m] = sum_k W[n][k] * A[m][k], so that
+// the operand that needs work before it can be multiplied -- the packed weight -- is the MMA's
+// A operand and lives in tensor memory, while the activations stream in by TMA:
+//   - dequant warps read the packed weight rows of a 128-channel tile straight from global
+//     memory, rebuild w = q * scale + offset in float32 (one rounding to the activation's 16-bit
+//     type) and write them into a TMEM stage with tcgen05.st (no shared-memory traffic);
+//   - a TMA warp loads the matching 64-wide K slice of A (up to 256 rows, 128-byte swizzle)
+//     into a shared-memory stage;
+//   - one thread issues tcgen05.mma (kind::f16, M = 128, N = tile rows of A, K = 16 per
+//     instruction) with A from TMEM and B from shared memory, accumulating in TMEM, and
+//     commits each stage back to the producers;
+//   - after the last stage the dequant warps read the accumulator with tcgen05.ld and store C.
+// W4A8 ("W4 解包为 INT8 ... S8×S8→S32", «测试用例与注册机制») uses the same kernel with the 4-bit
+// codes as exact f16 integers and the activation codes as exact f16 integers: every product is
+// an integer below 2^11 and every partial sum an integer below 2^24, so the float32 tensor-core
+// accumulation is exact and equals the int32 sum; the epilogue then either stores it as int32
+// or applies as * (ws * acc + off * rowsum).
+//
+// Every wait on an mbarrier is bounded: a wait that runs out sets the library's status word and
+// an abort flag, all roles leave their loops, in-flight work is drained (bounded) and TMEM is
+// freed before the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "internal.h"
 
 namespace qg {
 
 // Set (bitwise OR) by a kernel that gave up a bounded wait; read and cleared by qgemm_status.
 __device__ unsigned int g_status_word;
+
+namespace pf {
+
+constexpr int kBM = 128;              // output channels per tile (MMA M)
+constexpr int kBK = 64;               // K per pipeline stage
+constexpr int kStages = 4;
+constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
+constexpr int kStageBytesX = kMaxBN * kBK * 2;
+constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
+constexpr int kThreads = kWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kAccCol = 0;            // accumulator columns [0, BN)
+constexpr int kACol = 256;            // A stages: columns [256 + 32 s, 256 + 32 s + 32)
+constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at GB300 clocks
+constexpr unsigned kStatusTimeout = 1u;
+
+enum Wf { WF_INT4 = 0, WF_INT8 = 1, WF_FLOAT = 2, WF_CODES4 = 3 };
+enum Epi { EPI_STORE = 0, EPI_W4A8 = 1, EPI_ACC = 2 };
+
+struct Params {
+    int M, K, N, block, nb, BN;
+    const uint8_t* Bp;
+    const float* T;
+    void* C;
+    const float* a_scale;     // W4A8: per-row activation scale
+    const int32_t* rowsum;    // W4A8: per-row sum of activation codes
+    int32_t* acc;             // EPI_ACC output
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Waits for the phase of `parity` to complete; gives up after ~1 s or when another role has
+// aborted. Returns false if it gave up (and then raises the abort flag).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitCycles) {
+                *abort_flag = 1;
+                atomicOr(&g_status_word, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (TMEM) (+)= A (TMEM) x B (shared memory, descriptor)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+            d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte swizzle: rows of
+// 128 bytes (64 16-bit elements), 8-row swizzle atoms 1024 bytes apart (stride byte offset),
+// descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D float32, A and B both f16 (0) or both bf16 (1), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_f16(bool bf16, int n, int m) {
+    const uint32_t ab = bf16 ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    uint32_t d;
+    if (bf16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float u2f(uint32_t small) {   // exact for 0 <= small < 2^23
+    return __uint_as_float(0x4B000000u | small) - 8388608.0f;
+}
+
+// The 32 weights (k = k0 .. k0 + 31 of one channel row) this thread converts for one stage,
+// as 16 packed 16-bit pairs (low half = even k). raw holds the packed bytes.
+template <int WF, bool BF>
+__device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float o, uint32_t (&out)[16]) {
+    if constexpr (WF == WF_INT4 || WF == WF_CODES4) {
+        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};   // 32 nibbles
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float q0 = u2f((w[i] >> (8 * j)) & 15u), q1 = u2f((w[i] >> (8 * j + 4)) & 15u);
+                if constexpr (WF == WF_CODES4)
+                    out[4 * i + j] = pack2(q0, q1, BF);
+                else
+                    out[4 * i + j] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
+            }
+        }
+    } else if constexpr (WF == WF_INT8) {
+        const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q0 = u2f(w[i] & 255u), q1 = u2f((w[i] >> 8) & 255u);
+            const float q2 = u2f((w[i] >> 16) & 255u), q3 = u2f(w[i] >> 24);
+            out[2 * i] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
+            out[2 * i + 1] = pack2(fmaf(q2, s, o), fmaf(q3, s, o), BF);
+        }
+    } else {
+        const uint32_t w[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
+                                raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) out[i] = w[i];
+    }
+}
+
+template <int WF>
+__device__ __forceinline__ void load_raw(const uint8_t* row, int k0, uint4 (&raw)[4]) {
+    // bytes of k0 .. k0 + 31 of one packed row
+    constexpr int kBytes = (WF == WF_INT4 || WF == WF_CODES4) ? 16 : (WF == WF_INT8 ? 32 : 64);
+    const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)k0 * kBytes / 32);
+#pragma unroll
+    for (int i = 0; i < kBytes / 16; ++i) raw[i] = __ldg(src + i);
+}
+
+template <int CDT>
+__device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
+    if constexpr (CDT == DT_F32)
+        static_cast<float*>(C)[idx] = v;
+    else if constexpr (CDT == DT_F16)
+        static_cast<__half*>(C)[idx] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+}
+
+// One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), all of K.
+template <int WF, bool BF, int EPI, int CDT>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a, Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BN = p.BN;
+    const int n_tile = blockIdx.x * kBM, m_tile = blockIdx.y * BN;
+    const int nk = p.K / kBK;
+
+    uint8_t* xs = smem;   // kStages x [BN rows][128 B], 1024-byte aligned
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytesX);
+    // bars: full_x[kStages] | full_a[kStages] | empty[kStages] | acc_full
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t xs_s = smem_u32(xs);
+    auto full_x = [&](int s) { return smem_u32(bars + s); };
+    auto full_a = [&](int s) { return smem_u32(bars + kStages + s); };
+    auto empty = [&](int s) { return smem_u32(bars + 2 * kStages + s); };
+    const uint32_t acc_full = smem_u32(bars + 3 * kStages);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_x(s), 1);
+            mbar_init(full_a(s), 8);   // one arrival per dequant warp
+            mbar_init(empty(s), 1);    // one tcgen05.commit per use
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: the A (activation) slice of each stage
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)BN * kBK * 2;
+            int issued = 0;
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+                mbar_expect_tx(full_x(s), bytes);
+                tma_load_2d(xs_s + s * kStageBytesX, &tmap_a, ks * kBK, m_tile, full_x(s));
+                issued = ks + 1;
+            }
+            if (*abort_flag) {   // let the copies already issued land before the block exits
+                for (int ks = issued - kStages < 0 ? 0 : issued - kStages; ks < issued; ++ks) {
+                    volatile int never = 0;
+                    mbar_wait(full_x(ks % kStages), (uint32_t)(ks / kStages) & 1u, &never);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BF, BN, kBM);
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+                if (!mbar_wait(full_a(s), ph, abort_flag)) break;
+                if (!mbar_wait(full_x(s), ph, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t bdesc = sw128_desc(xs_s + s * kStageBytesX);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_ts(tmem + kAccCol, tmem + kACol + s * (kBK / 2) + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
+                           (ks | kk) != 0);
+                mma_commit(empty(s));
+            }
+            mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
+        }
+    } else {
+        // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each stage
+        const int q = warp & 3, h = (warp - 2) >> 2;
+        const int row = n_tile + 32 * q + lane;
+        const int rc = row < p.N ? row : p.N - 1;
+        constexpr int kRowBytes32 = (WF == WF_INT4 || WF == WF_CODES4) ? 16 : (WF == WF_INT8 ? 32 : 64);
+        const uint8_t* wrow = p.Bp + (size_t)rc * ((size_t)p.K / 32 * kRowBytes32);
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        // the next stage's raw weight bytes are fetched while the current stage is converted
+        uint4 cur[4], nxt[4];
+        float cs = 1.f, co = 0.f, nsc = 1.f, nof = 0.f;
+        auto fetch = [&](int ks, uint4 (&raw)[4], float& sc, float& of) {
+            const int k0 = ks * kBK + 32 * h;
+            load_raw<WF>(wrow, k0, raw);
+            if constexpr (WF == WF_INT4 || WF == WF_INT8) {
+                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + ((size_t)rc * p.nb + k0 / p.block) * 2));
+                of = t.x;
+                sc = t.y;
+            }
+        };
+        if (nk > 0) fetch(0, cur, cs, co);
+        for (int ks = 0; ks < nk; ++ks) {
+            const int s = ks % kStages;
+            const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+            if (ks + 1 < nk) fetch(ks + 1, nxt, nsc, nof);
+            uint32_t out[16];
+            convert32<WF, BF>(cur, cs, co, out);
+            if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+            tc_fence_after();
+            tmem_st16(tmem + lane_base + kACol + s * (kBK / 2) + 16 * h, out);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_a(s));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+            cs = nsc;
+            co = nof;
+        }
+        // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2)
+        const bool ok = mbar_wait(acc_full, 0u, abort_flag) && !*abort_flag;
+        tc_fence_after();
+        if (ok) {
+            float ws = 0.f, wo = 0.f;
+            if constexpr (EPI == EPI_W4A8) {
+                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + (size_t)rc * 2));
+                wo = t.x;
+                ws = t.y;
+            }
+            for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kAccCol + c0, v);
+                tmem_ld_wait();
+                if (row < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = m_tile + c0 + i;
+                        if (m < p.M) {
+                            const float d = __uint_as_float(v[i]);
+                            const size_t idx = (size_t)m * p.N + row;
+                            if constexpr (EPI == EPI_ACC) {
+                                p.acc[idx] = __float2int_rn(d);
+                            } else if constexpr (EPI == EPI_W4A8) {
+                                // d is the exact integer accumulator (see the file comment)
+                                const float rs = (float)__ldg(p.rowsum + m);
+                                store_c<CDT>(p.C, idx, __ldg(p.a_scale + m) * fmaf(ws, d, wo * rs));
+                            } else {
+                                store_c<CDT>(p.C, idx, d);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- W4A8 activation codes as f16
+__global__ void codes_to_f16_kernel(const int8_t* __restrict__ qa, __half* __restrict__ out, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        out[i] = __int2half_rn(qa[i]);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// [M][K] 16-bit activations, box of 64 (K) x BN (rows), 128-byte swizzle; rows past M read 0.
+cudaError_t make_tmap(CUtensorMap* map, const void* A, bool bf16, int M, int K, int BN) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)BN};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                           const_cast<void*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int pick_bn(int M) {
+    if (M >= 256) return 256;
+    return (M + 63) / 64 * 64;
+}
+
+size_t smem_bytes() { return (size_t)kStages * kStageBytesX + 256; }
+
+template <int WF, bool BF, int EPI, int CDT>
+cudaError_t launch_k(const CUtensorMap& map, const Params& p, cudaStream_t s) {
+    auto kern = prefill_kernel<WF, BF, EPI, CDT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes());
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN);
+    kern<<<grid, kThreads, smem_bytes(), s>>>(map, p);
+    return cudaGetLastError();
+}
+
+template <int WF, bool BF, int EPI>
+cudaError_t launch_cdt(const CUtensorMap& map, const Params& p, int c_dtype, cudaStream_t s) {
+    switch (c_dtype) {
+        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(map, p, s);
+        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(map, p, s);
+        default: return launch_k<WF, BF, EPI, DT_BF16>(map, p, s);
+    }
+}
+
+}  // namespace pf
 
 cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
     unsigned int h = 0;
@@ -20,8 +472,50 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
     return e;
 }
 
-bool prefill_supported(int, int, int, int, int) { return false; }
-cudaError_t launch_prefill(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_w4a8_gemm(const W4A8Args&, cudaStream_t) { return cudaErrorNotSupported; }
+bool prefill_supported(int M, int K, int N, int fmt, int a_dtype) {
+    (void)K;
+    (void)N;
+    (void)fmt;
+    return M > 16 && (a_dtype == DT_F16 || a_dtype == DT_BF16);
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
+    pf::Params p{};
+    p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.block; p.nb = a.K / a.block;
+    p.BN = pf::pick_bn(a.M);
+    p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
+    const bool bf = a.a_dtype == DT_BF16;
+    CUtensorMap map;
+    cudaError_t e = pf::make_tmap(&map, a.A, bf, a.M, a.K, p.BN);
+    if (e != cudaSuccess) return e;
+    if (a.fmt == FMT_INT4)
+        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
+    if (a.fmt == FMT_INT8)
+        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
+    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
+              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
+}
+
+cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
+    pf::Params p{};
+    p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.K; p.nb = 1;
+    p.BN = pf::pick_bn(a.M);
+    p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
+    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc;
+    CUtensorMap map;
+    cudaError_t e = pf::make_tmap(&map, a.qa16, false, a.M, a.K, p.BN);
+    if (e != cudaSuccess) return e;
+    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(map, p, s);
+    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(map, p, a.c_dtype, s);
+}
+
+cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s) {
+    const int threads = 256;
+    const size_t want = (n + threads - 1) / threads;
+    pf::codes_to_f16_kernel<<<(int)(want < 8192 ? want : 8192), threads, 0, s>>>(qa, static_cast<__half*>(out), n);
+    return cudaGetLastError();
+}
 
 }  // namespace qg

@@ -52,9 +52,10 @@ size_t packed_bytes(int K, int N, int mode, int w_dtype) {
     }
 }
 
-// W4A8 workspace: qa [M][K] int8, then as [M] f32 and rowsum [M] int32, each 256-B aligned.
+// W4A8 workspace: the activation codes as f16 [M][K] (exact integers, the tensor cores' operand
+// type), then as [M] f32 and rowsum [M] int32, each 256-byte aligned.
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-size_t w4a8_ws(int M, int K) { return align256((size_t)M * K) + align256((size_t)M * 4) * 2; }
+size_t w4a8_ws(int M, int K) { return align256((size_t)M * K * 2) + align256((size_t)M * 4) * 2; }
 
 // Kernel choice by shape (one backend: these are all this library's CUDA kernels).
 enum Path { PATH_F32, PATH_DECODE, PATH_PREFILL };
@@ -154,12 +155,12 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
     cudaError_t e;
 
     if (mode == QGEMM_MODE_W4A8) {
-        int8_t* qa = static_cast<int8_t*>(workspace);
-        float* as = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)M * K));
+        void* qa16 = workspace;
+        float* as = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)M * K * 2));
         int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
-        e = qg::launch_act_quant(M, K, A, a_dtype, qa, as, rs, s);
+        e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
         if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-        qg::W4A8Args w{M, K, N, qa, as, rs, Bp, T, nullptr, C, c_dtype};
+        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype};
         e = qg::launch_w4a8_gemm(w, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
     }
@@ -196,21 +197,35 @@ int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float*
     if (!A || !qa || !a_scale || !rowsum) return fail(QGEMM_ERR_ARG, "null pointer");
     if (!aligned16(A) || !aligned16(qa) || !aligned16(a_scale) || !aligned16(rowsum))
         return fail(QGEMM_ERR_ALIGN, "pointers must be 16-byte aligned");
-    cudaError_t e = qg::launch_act_quant(M, K, A, a_dtype, qa, a_scale, rowsum, static_cast<cudaStream_t>(stream));
+    cudaError_t e =
+        qg::launch_act_quant(M, K, A, a_dtype, qa, nullptr, a_scale, rowsum, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "act_quant launch");
 }
 
-int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* stream) {
+size_t qgemm_w4a8_acc_workspace_bytes(int M, int K) {
+    if (M <= 0 || K <= 0) return 0;
+    return (size_t)M * K * 2;
+}
+
+int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* workspace,
+                   size_t workspace_bytes, void* stream) {
     int block = 0;
     int rc = check_shape(K, N, QGEMM_MODE_W4A8, &block);
     if (rc != QGEMM_OK) return rc;
     if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
     if (M == 0 || N == 0) return QGEMM_OK;
     if (!qa || !Bp || !acc) return fail(QGEMM_ERR_ARG, "null pointer");
-    if (!aligned16(qa) || !aligned16(Bp) || !aligned16(acc))
+    if (!aligned16(qa) || !aligned16(Bp) || !aligned16(acc) || (workspace && !aligned16(workspace)))
         return fail(QGEMM_ERR_ALIGN, "pointers must be 16-byte aligned");
-    qg::W4A8Args w{M, K, N, qa, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
-    cudaError_t e = qg::launch_w4a8_gemm(w, static_cast<cudaStream_t>(stream));
+    const size_t need = qgemm_w4a8_acc_workspace_bytes(M, K);
+    if (!workspace || workspace_bytes < need)
+        return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = qg::launch_codes_to_f16(qa, workspace, (size_t)M * K, s);
+    if (e != cudaSuccess) return cuda_fail(e, "codes_to_f16 launch");
+    qg::W4A8Args w{M, K, N, workspace, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
+    e = qg::launch_w4a8_gemm(w, s);
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
 }
 
