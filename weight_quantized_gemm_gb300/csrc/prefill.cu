@@ -44,7 +44,7 @@ constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + 
 constexpr int kThreads = kWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;            // accumulator columns [0, BN)
-constexpr int kACol = 256;            // A stages: columns [256 + 32 s, 256 + 32 s + 32)
+constexpr int kACol = 256;            // A stages from column 256: 32 columns each (64 with a low part)
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at GB300 clocks
 constexpr unsigned kStatusTimeout = 1u;
 
@@ -178,10 +178,29 @@ __device__ __forceinline__ float u2f(uint32_t small) {   // exact for 0 <= small
     return __uint_as_float(0x4B000000u | small) - 8388608.0f;
 }
 
-// The 32 weights (k = k0 .. k0 + 31 of one channel row) this thread converts for one stage,
-// as 16 packed 16-bit pairs (low half = even k). raw holds the packed bytes.
+// Dequantized weights with bf16 activations are split as w = hi + lo with hi = bf16(w) and
+// lo = bf16(w - hi): the MMA then multiplies both parts, which keeps the weight to about 2^-17
+// relative instead of bf16's 2^-9 (f16 weights are kept to 2^-12 by one rounding).
 template <int WF, bool BF>
-__device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float o, uint32_t (&out)[16]) {
+struct Split {
+    static constexpr bool kOn = BF && (WF == WF_INT4 || WF == WF_INT8);
+    static constexpr int kStageCols = kOn ? 64 : 32;
+};
+
+__device__ __forceinline__ uint32_t pack2_split(float lo, float hi, uint32_t& rest) {
+    const uint32_t h = pack2(lo, hi, true);
+    const float l0 = lo - __uint_as_float(h << 16), l1 = hi - __uint_as_float(h & 0xFFFF0000u);
+    rest = pack2(l0, l1, true);
+    return h;
+}
+
+// The 32 weights (k = k0 .. k0 + 31 of one channel row) this thread converts for one stage,
+// as 16 packed 16-bit pairs (low half = even k); with Split, rest gets the low parts. raw holds
+// the packed bytes.
+template <int WF, bool BF>
+__device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float o, uint32_t (&out)[16],
+                                          uint32_t (&rest)[16]) {
+    constexpr bool kSplit = Split<WF, BF>::kOn;
     if constexpr (WF == WF_INT4 || WF == WF_CODES4) {
         const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};   // 32 nibbles
 #pragma unroll
@@ -191,6 +210,8 @@ __device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float 
                 const float q0 = u2f((w[i] >> (8 * j)) & 15u), q1 = u2f((w[i] >> (8 * j + 4)) & 15u);
                 if constexpr (WF == WF_CODES4)
                     out[4 * i + j] = pack2(q0, q1, BF);
+                else if constexpr (kSplit)
+                    out[4 * i + j] = pack2_split(fmaf(q0, s, o), fmaf(q1, s, o), rest[4 * i + j]);
                 else
                     out[4 * i + j] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
             }
@@ -201,8 +222,13 @@ __device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float 
         for (int i = 0; i < 8; ++i) {
             const float q0 = u2f(w[i] & 255u), q1 = u2f((w[i] >> 8) & 255u);
             const float q2 = u2f((w[i] >> 16) & 255u), q3 = u2f(w[i] >> 24);
-            out[2 * i] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
-            out[2 * i + 1] = pack2(fmaf(q2, s, o), fmaf(q3, s, o), BF);
+            if constexpr (kSplit) {
+                out[2 * i] = pack2_split(fmaf(q0, s, o), fmaf(q1, s, o), rest[2 * i]);
+                out[2 * i + 1] = pack2_split(fmaf(q2, s, o), fmaf(q3, s, o), rest[2 * i + 1]);
+            } else {
+                out[2 * i] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
+                out[2 * i + 1] = pack2(fmaf(q2, s, o), fmaf(q3, s, o), BF);
+            }
         }
     } else {
         const uint32_t w[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
@@ -295,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(BF, BN, kBM);
+            constexpr int kCols = Split<WF, BF>::kStageCols;
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
@@ -303,9 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 tc_fence_after();
                 const uint64_t bdesc = sw128_desc(xs_s + s * kStageBytesX);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_ts(tmem + kAccCol, tmem + kACol + s * (kBK / 2) + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
                            (ks | kk) != 0);
+                    if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
+                        mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + 32 + kk * 8, bdesc + (uint64_t)(2 * kk),
+                               idesc, 1u);
+                }
                 mma_commit(empty(s));
             }
             mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
@@ -335,11 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int s = ks % kStages;
             const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
             if (ks + 1 < nk) fetch(ks + 1, nxt, nsc, nof);
-            uint32_t out[16];
-            convert32<WF, BF>(cur, cs, co, out);
+            uint32_t out[16], rest[16];
+            convert32<WF, BF>(cur, cs, co, out, rest);
             if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
             tc_fence_after();
-            tmem_st16(tmem + lane_base + kACol + s * (kBK / 2) + 16 * h, out);
+            constexpr int kCols = Split<WF, BF>::kStageCols;
+            tmem_st16(tmem + lane_base + kACol + s * kCols + 16 * h, out);
+            if constexpr (Split<WF, BF>::kOn) tmem_st16(tmem + lane_base + kACol + s * kCols + 32 + 16 * h, rest);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
