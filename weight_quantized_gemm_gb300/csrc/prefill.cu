@@ -128,6 +128,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, u
         "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D (TMEM) (+)= A (shared memory, descriptor) x B (shared memory, descriptor)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ uint4 lds128u(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -174,9 +187,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
     return d;
 }
-__device__ __forceinline__ float u2f(uint32_t small) {   // exact for 0 <= small < 2^23
-    return __uint_as_float(0x4B000000u | small) - 8388608.0f;
-}
 
 // Dequantized weights with bf16 activations are split as w = hi + lo with hi = bf16(w) and
 // lo = bf16(w - hi): the MMA then multiplies both parts, which keeps the weight to about 2^-17
@@ -194,6 +204,35 @@ __device__ __forceinline__ uint32_t pack2_split(float lo, float hi, uint32_t& re
     return h;
 }
 
+// Exact float32 values of 4- and 8-bit codes without an integer conversion: a code placed in
+// mantissa bits 15..18 of the float 256.0 reads 256 + q, in bits 19..22 of 16.0 it reads 16 + q,
+// and an 8-bit code in bits 15..22 of 256.0 reads 256 + q. The bias folds into the offset, so
+// w = q * s + o = fma(bias + q, s, o - bias * s) is a single rounding of the exact value plus the
+// rounding of o - bias * s (at most 2^-24 * (|o| + 256 s), which is negligible).
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+    return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+// (x0, x1) * (s, s) + (c0, c1) in one packed float32 instruction
+__device__ __forceinline__ void fma2(float x0, float x1, float s, float c0, float c1, float& r0, float& r1) {
+    asm("{\n\t.reg .b64 x, y, z, d;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %6};\n\t"
+        "fma.rn.f32x2 d, x, y, z;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(x0), "f"(x1), "f"(s), "f"(c0), "f"(c1));
+}
+// byte j of w moved to bits 15..22
+template <int J>
+__device__ __forceinline__ uint32_t byte_to_15(uint32_t w) {
+    if constexpr (8 * J < 15) return w << (15 - 8 * J);
+    else return w >> (8 * J - 15);
+}
+
 // The 32 weights (k = k0 .. k0 + 31 of one channel row) this thread converts for one stage,
 // as 16 packed 16-bit pairs (low half = even k); with Split, rest gets the low parts. raw holds
 // the packed bytes.
@@ -201,34 +240,52 @@ template <int WF, bool BF>
 __device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float o, uint32_t (&out)[16],
                                           uint32_t (&rest)[16]) {
     constexpr bool kSplit = Split<WF, BF>::kOn;
-    if constexpr (WF == WF_INT4 || WF == WF_CODES4) {
-        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};   // 32 nibbles
+    auto emit = [&](int idx, float w0, float w1) {
+        if constexpr (kSplit) out[idx] = pack2_split(w0, w1, rest[idx]);
+        else out[idx] = pack2(w0, w1, BF);
+    };
+    if constexpr (WF == WF_INT4) {
+        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};   // 32 nibbles, byte j = (k 2j, 2j+1)
+        const float c_lo = fmaf(-256.f, s, o), c_hi = fmaf(-16.f, s, o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t t[4] = {byte_to_15<0>(w[i]), byte_to_15<1>(w[i]), byte_to_15<2>(w[i]), byte_to_15<3>(w[i])};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float q0 = __uint_as_float(lop3_and_or(t[j], 0x00078000u, 0x43800000u));   // 256 + low nibble
+                const float q1 = __uint_as_float(lop3_and_or(t[j], 0x00780000u, 0x41800000u));   // 16 + high nibble
+                float w0, w1;
+                fma2(q0, q1, s, c_lo, c_hi, w0, w1);
+                emit(4 * i + j, w0, w1);
+            }
+        }
+    } else if constexpr (WF == WF_CODES4) {
+        // the codes themselves, exact in f16: (1024 + lo, 1024 + 16 hi) -> (lo, hi)
+        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float q0 = u2f((w[i] >> (8 * j)) & 15u), q1 = u2f((w[i] >> (8 * j + 4)) & 15u);
-                if constexpr (WF == WF_CODES4)
-                    out[4 * i + j] = pack2(q0, q1, BF);
-                else if constexpr (kSplit)
-                    out[4 * i + j] = pack2_split(fmaf(q0, s, o), fmaf(q1, s, o), rest[4 * i + j]);
-                else
-                    out[4 * i + j] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
+                const uint32_t v = lop3_and_or(prmt(w[i], w[i], 0x4040u + 0x0101u * j), 0x00F0000Fu, 0x64006400u);
+                uint32_t d;
+                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(v), "r"(0x2C003C00u), "r"(0xD400E400u));
+                out[4 * i + j] = d;
             }
         }
     } else if constexpr (WF == WF_INT8) {
         const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+        const float c8 = fmaf(-256.f, s, o);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float q0 = u2f(w[i] & 255u), q1 = u2f((w[i] >> 8) & 255u);
-            const float q2 = u2f((w[i] >> 16) & 255u), q3 = u2f(w[i] >> 24);
-            if constexpr (kSplit) {
-                out[2 * i] = pack2_split(fmaf(q0, s, o), fmaf(q1, s, o), rest[2 * i]);
-                out[2 * i + 1] = pack2_split(fmaf(q2, s, o), fmaf(q3, s, o), rest[2 * i + 1]);
-            } else {
-                out[2 * i] = pack2(fmaf(q0, s, o), fmaf(q1, s, o), BF);
-                out[2 * i + 1] = pack2(fmaf(q2, s, o), fmaf(q3, s, o), BF);
-            }
+            const float q0 = __uint_as_float(lop3_and_or(byte_to_15<0>(w[i]), 0x007F8000u, 0x43800000u));
+            const float q1 = __uint_as_float(lop3_and_or(byte_to_15<1>(w[i]), 0x007F8000u, 0x43800000u));
+            const float q2 = __uint_as_float(lop3_and_or(byte_to_15<2>(w[i]), 0x007F8000u, 0x43800000u));
+            const float q3 = __uint_as_float(lop3_and_or(byte_to_15<3>(w[i]), 0x007F8000u, 0x43800000u));
+            float w0, w1, w2, w3;
+            fma2(q0, q1, s, c8, c8, w0, w1);
+            fma2(q2, q3, s, c8, c8, w2, w3);
+            emit(2 * i, w0, w1);
+            emit(2 * i + 1, w2, w3);
         }
     } else {
         const uint32_t w[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
@@ -236,15 +293,6 @@ __device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float 
 #pragma unroll
         for (int i = 0; i < 16; ++i) out[i] = w[i];
     }
-}
-
-template <int WF>
-__device__ __forceinline__ void load_raw(const uint8_t* row, int k0, uint4 (&raw)[4]) {
-    // bytes of k0 .. k0 + 31 of one packed row
-    constexpr int kBytes = (WF == WF_INT4 || WF == WF_CODES4) ? 16 : (WF == WF_INT8 ? 32 : 64);
-    const uint4* src = reinterpret_cast<const uint4*>(row + (size_t)k0 * kBytes / 32);
-#pragma unroll
-    for (int i = 0; i < kBytes / 16; ++i) raw[i] = __ldg(src + i);
 }
 
 template <int CDT>
@@ -257,21 +305,37 @@ __device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
         static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
 }
 
+// Shared-memory stage: the A (activation) box [BN rows][128 B] at offset 0 and the packed
+// weight box at kWOff: [128 rows][stage bytes of one row] for the quantized formats, or the
+// 16-bit weights [128 rows][128 B] with the 128-byte swizzle in float mode (then read by the
+// MMA directly as its A operand).
+constexpr int kWOff = kStageBytesX;
+constexpr int kWBytesMax = kBM * kBK * 2;
+constexpr int kStageBytes = kStageBytesX + kWBytesMax;
+template <int WF>
+struct WBox {
+    static constexpr int kRowBytes = (WF == WF_INT4 || WF == WF_CODES4) ? kBK / 2 : (WF == WF_INT8 ? kBK : 2 * kBK);
+};
+
 // One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), all of K.
 template <int WF, bool BF, int EPI, int CDT>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a, Params p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                                              const __grid_constant__ CUtensorMap tmap_w, Params p) {
+    constexpr bool kDequant = WF != WF_FLOAT;          // weights go through the dequant warps into TMEM
+    constexpr bool kTable = WF == WF_INT4 || WF == WF_INT8;
+    constexpr int kCols = Split<WF, BF>::kStageCols;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BN = p.BN;
     const int n_tile = blockIdx.x * kBM, m_tile = blockIdx.y * BN;
     const int nk = p.K / kBK;
 
-    uint8_t* xs = smem;   // kStages x [BN rows][128 B], 1024-byte aligned
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytesX);
-    // bars: full_x[kStages] | full_a[kStages] | empty[kStages] | acc_full
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    // bars: full[kStages] (both boxes landed) | full_a[kStages] (TMEM A stage written) |
+    //       empty[kStages] (MMAs of the stage done) | acc_full
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const uint32_t xs_s = smem_u32(xs);
+    const uint32_t st_s = smem_u32(smem);
     auto full_x = [&](int s) { return smem_u32(bars + s); };
     auto full_a = [&](int s) { return smem_u32(bars + kStages + s); };
     auto empty = [&](int s) { return smem_u32(bars + 2 * kStages + s); };
@@ -287,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -298,16 +363,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- TMA producer: the A (activation) slice of each stage
+        // ---------------- TMA producer: the A slice and the weight slice of each stage
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)BN * kBK * 2;
+            const uint32_t bytes = (uint32_t)BN * kBK * 2 + (uint32_t)kBM * WBox<WF>::kRowBytes;
             int issued = 0;
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(full_x(s), bytes);
-                tma_load_2d(xs_s + s * kStageBytesX, &tmap_a, ks * kBK, m_tile, full_x(s));
+                tma_load_2d(st_s + s * kStageBytes, &tmap_a, ks * kBK, m_tile, full_x(s));
+                // weight box: x in bytes for the packed formats, in elements for float mode
+                tma_load_2d(st_s + s * kStageBytes + kWOff, &tmap_w,
+                            WF == WF_FLOAT ? ks * kBK : ks * WBox<WF>::kRowBytes, n_tile, full_x(s));
                 issued = ks + 1;
             }
             if (*abort_flag) {   // let the copies already issued land before the block exits
@@ -321,21 +389,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(BF, BN, kBM);
-            constexpr int kCols = Split<WF, BF>::kStageCols;
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
-                if (!mbar_wait(full_a(s), ph, abort_flag)) break;
+                if constexpr (kDequant)
+                    if (!mbar_wait(full_a(s), ph, abort_flag)) break;
                 if (!mbar_wait(full_x(s), ph, abort_flag)) break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_desc(xs_s + s * kStageBytesX);
+                const uint64_t bdesc = sw128_desc(st_s + s * kStageBytes);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
-                           (ks | kk) != 0);
-                    if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
-                        mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + 32 + kk * 8, bdesc + (uint64_t)(2 * kk),
-                               idesc, 1u);
+                    if constexpr (kDequant) {
+                        mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
+                               (ks | kk) != 0);
+                        if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
+                            mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + 32 + kk * 8, bdesc + (uint64_t)(2 * kk),
+                                   idesc, 1u);
+                    } else {
+                        const uint64_t adesc = sw128_desc(st_s + s * kStageBytes + kWOff);
+                        mma_ss(tmem + kAccCol, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                               (ks | kk) != 0);
+                    }
                 }
                 mma_commit(empty(s));
             }
@@ -344,43 +418,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else {
         // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each stage
         const int q = warp & 3, h = (warp - 2) >> 2;
-        const int row = n_tile + 32 * q + lane;
+        const int r = 32 * q + lane;                 // row inside the tile
+        const int row = n_tile + r;
         const int rc = row < p.N ? row : p.N - 1;
-        constexpr int kRowBytes32 = (WF == WF_INT4 || WF == WF_CODES4) ? 16 : (WF == WF_INT8 ? 32 : 64);
-        const uint8_t* wrow = p.Bp + (size_t)rc * ((size_t)p.K / 32 * kRowBytes32);
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        // the next stage's raw weight bytes are fetched while the current stage is converted
-        uint4 cur[4], nxt[4];
-        float cs = 1.f, co = 0.f, nsc = 1.f, nof = 0.f;
-        auto fetch = [&](int ks, uint4 (&raw)[4], float& sc, float& of) {
-            const int k0 = ks * kBK + 32 * h;
-            load_raw<WF>(wrow, k0, raw);
-            if constexpr (WF == WF_INT4 || WF == WF_INT8) {
-                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + ((size_t)rc * p.nb + k0 / p.block) * 2));
-                of = t.x;
-                sc = t.y;
-            }
-        };
-        if (nk > 0) fetch(0, cur, cs, co);
-        for (int ks = 0; ks < nk; ++ks) {
-            const int s = ks % kStages;
-            const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
-            if (ks + 1 < nk) fetch(ks + 1, nxt, nsc, nof);
-            uint32_t out[16], rest[16];
-            convert32<WF, BF>(cur, cs, co, out, rest);
-            if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-            tc_fence_after();
-            constexpr int kCols = Split<WF, BF>::kStageCols;
-            tmem_st16(tmem + lane_base + kACol + s * kCols + 16 * h, out);
-            if constexpr (Split<WF, BF>::kOn) tmem_st16(tmem + lane_base + kACol + s * kCols + 32 + 16 * h, rest);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full_a(s));
+        if constexpr (kDequant) {
+            // {offset, scale} of the stages ks .. ks + 3, shifted along as the stages advance
+            float2 tq[4];
+            auto table = [&](int ks) {
+                if constexpr (kTable) {
+                    if (ks < nk)
+                        return __ldg(reinterpret_cast<const float2*>(
+                            p.T + ((size_t)rc * p.nb + (ks * kBK + 32 * h) / p.block) * 2));
+                }
+                return make_float2(0.f, 1.f);
+            };
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
-            cs = nsc;
-            co = nof;
+            for (int i = 0; i < 4; ++i) tq[i] = table(i);
+            for (int ks = 0; ks < nk; ++ks) {
+                const int s = ks % kStages;
+                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+                if (!mbar_wait(full_x(s), ph, abort_flag)) break;
+                const uint32_t wsrc = st_s + s * kStageBytes + kWOff + r * WBox<WF>::kRowBytes +
+                                      h * (WBox<WF>::kRowBytes / 2);
+                uint4 raw[4];
+                raw[0] = lds128u(wsrc);
+                if constexpr (WF == WF_INT8) raw[1] = lds128u(wsrc + 16);
+                uint32_t out[16], rest[16];
+                convert32<WF, BF>(raw, tq[0].y, tq[0].x, out, rest);
+                tq[0] = tq[1];
+                tq[1] = tq[2];
+                tq[2] = tq[3];
+                tq[3] = table(ks + 4);
+                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                tmem_st16(tmem + lane_base + kACol + s * kCols + 16 * h, out);
+                if constexpr (Split<WF, BF>::kOn) tmem_st16(tmem + lane_base + kACol + s * kCols + 32 + 16 * h, rest);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_a(s));
+            }
         }
         // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2)
         const bool ok = mbar_wait(acc_full, 0u, abort_flag) && !*abort_flag;
@@ -469,24 +547,52 @@ int pick_bn(int M) {
     return (M + 63) / 64 * 64;
 }
 
-size_t smem_bytes() { return (size_t)kStages * kStageBytesX + 256; }
+size_t smem_bytes() { return (size_t)kStages * kStageBytes + 256; }
+
+// The packed weight rows [N][row bytes] as a 2-D byte (quantized formats) or 16-bit (float mode,
+// 128-byte swizzle) tensor; box = one stage of 128 rows; rows past N read 0.
+cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N, int K) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUresult r;
+    if (wf == WF_FLOAT) {
+        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(Bp),
+                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const int row_bytes = (wf == WF_INT8) ? K : K / 2;
+        const int box_bytes = (wf == WF_INT8) ? kBK : kBK / 2;
+        const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
+        const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kBM};
+        const cuuint32_t estr[2] = {1, 1};
+        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Bp), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 template <int WF, bool BF, int EPI, int CDT>
-cudaError_t launch_k(const CUtensorMap& map, const Params& p, cudaStream_t s) {
+cudaError_t launch_k(const CUtensorMap& amap, const CUtensorMap& wmap, const Params& p, cudaStream_t s) {
     auto kern = prefill_kernel<WF, BF, EPI, CDT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes());
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN);
-    kern<<<grid, kThreads, smem_bytes(), s>>>(map, p);
+    kern<<<grid, kThreads, smem_bytes(), s>>>(amap, wmap, p);
     return cudaGetLastError();
 }
 
 template <int WF, bool BF, int EPI>
-cudaError_t launch_cdt(const CUtensorMap& map, const Params& p, int c_dtype, cudaStream_t s) {
+cudaError_t launch_cdt(const CUtensorMap& amap, const CUtensorMap& wmap, const Params& p, int c_dtype, cudaStream_t s) {
     switch (c_dtype) {
-        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(map, p, s);
-        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(map, p, s);
-        default: return launch_k<WF, BF, EPI, DT_BF16>(map, p, s);
+        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(amap, wmap, p, s);
+        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(amap, wmap, p, s);
+        default: return launch_k<WF, BF, EPI, DT_BF16>(amap, wmap, p, s);
     }
 }
 
@@ -518,17 +624,19 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     const bool bf = a.a_dtype == DT_BF16;
-    CUtensorMap map;
-    cudaError_t e = pf::make_tmap(&map, a.A, bf, a.M, a.K, p.BN);
+    const int wf = a.fmt == FMT_INT4 ? pf::WF_INT4 : (a.fmt == FMT_INT8 ? pf::WF_INT8 : pf::WF_FLOAT);
+    CUtensorMap amap, wmap;
+    cudaError_t e = pf::make_tmap(&amap, a.A, bf, a.M, a.K, p.BN);
+    if (e == cudaSuccess) e = pf::make_wmap(&wmap, a.Bp, wf, bf, a.N, a.K);
     if (e != cudaSuccess) return e;
     if (a.fmt == FMT_INT4)
-        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
+        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
     if (a.fmt == FMT_INT8)
-        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
-    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(map, p, a.c_dtype, s)
-              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(map, p, a.c_dtype, s);
+        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
+    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
+              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
 }
 
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
@@ -537,11 +645,12 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc;
-    CUtensorMap map;
-    cudaError_t e = pf::make_tmap(&map, a.qa16, false, a.M, a.K, p.BN);
+    CUtensorMap amap, wmap;
+    cudaError_t e = pf::make_tmap(&amap, a.qa16, false, a.M, a.K, p.BN);
+    if (e == cudaSuccess) e = pf::make_wmap(&wmap, a.Bp, pf::WF_CODES4, false, a.N, a.K);
     if (e != cudaSuccess) return e;
-    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(map, p, s);
-    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(map, p, a.c_dtype, s);
+    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(amap, wmap, p, s);
+    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(amap, wmap, p, a.c_dtype, s);
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s) {
