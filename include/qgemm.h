@@ -128,6 +128,31 @@ int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_
 /* Workspace bytes qgemm_w4a8_acc needs (0 for invalid sizes). */
 size_t qgemm_w4a8_acc_workspace_bytes(int M, int K);
 
+/* ---------------------------------------------------------------- no-allocation variant */
+
+/* Size of the library's own scratch buffer used by qgemm_run_noalloc (4 MiB). */
+#define QGEMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* qgemm_run without a caller workspace, for callers that cannot hand the library device memory
+ * of their own: code whose execution path must not allocate (a plugin inside an inference
+ * engine that owns all device memory, a real-time loop that cannot pay for an allocator call,
+ * a C host with no device allocator at hand). The pages have no counterpart to this call; it is
+ * a convenience of this library.
+ * It computes exactly what qgemm_run computes, with the same kernels, but its scratch memory is
+ * a fixed array inside the library (QGEMM_NOALLOC_SCRATCH_BYTES, 256-byte aligned) that every
+ * GPU which loads the library keeps until the process exits. No call allocates or frees device
+ * memory.
+ *   - A call whose scratch need (qgemm_workspace_bytes) exceeds the array is rejected with
+ *     QGEMM_ERR_WORKSPACE before anything is enqueued. Calls that need no scratch always fit.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before capturing a stream into a graph.
+ *   - All calls share the one array and leave their data in it. Every byte a call reads from it
+ *     is written earlier by the same call, so nothing needs clearing; but two calls whose work
+ *     overlaps on the GPU (different streams, or different host threads, without ordering)
+ *     race on it and may produce wrong results. Order them on one stream. */
+int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                      const float* T, void* C, int c_dtype, void* stream);
+
 /* ---------------------------------------------------------------- options */
 
 /* QGEMM_OPT_LAUNCH_OVERLAP (default 0). When 1, the decode kernel (M <= 16) is launched with a

@@ -15,12 +15,13 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
 MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
 OPT_LAUNCH_OVERLAP = 1
+NOALLOC_SCRATCH_BYTES = 4 << 20
 F32, F16, BF16 = 0, 1, 2
 OK = 0
 ERRORS = {-1: "QGEMM_ERR_ARG", -2: "QGEMM_ERR_UNSUPPORTED", -3: "QGEMM_ERR_ALIGN", -4: "QGEMM_ERR_WORKSPACE",
@@ -41,6 +42,7 @@ SIGNATURES = {
     "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
     "qgemm_w4a8_acc_workspace_bytes": ([_I, _I], _SZ),
     "qgemm_status": ([_P], _I),
+    "qgemm_run_noalloc": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P], _I),
     "qgemm_set_option": ([_I, _I], _I),
     "qgemm_get_option": ([_I], _I),
     "qgemm_error_string": ([_I], ctypes.c_char_p),
@@ -117,6 +119,13 @@ def qgemm_run(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().qgemm_run(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(C), c_dtype,
                             _ptr(workspace), workspace_bytes, _stream(stream)), "qgemm_run")
+
+
+def qgemm_run_noalloc(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, C, c_dtype: int,
+                      stream=None) -> None:
+    """qgemm_run with the library's built-in scratch instead of a caller workspace (see qgemm.h)."""
+    _check(load().qgemm_run_noalloc(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(C), c_dtype,
+                                    _stream(stream)), "qgemm_run_noalloc")
 
 
 def qgemm_act_quant(M: int, K: int, A, a_dtype: int, qa, a_scale, rowsum, stream=None) -> None:

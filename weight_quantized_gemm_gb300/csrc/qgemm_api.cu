@@ -4,6 +4,7 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "../../include/qgemm.h"
 #include "internal.h"
@@ -237,6 +238,60 @@ int qgemm_status(void* stream) {
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (v != 0) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status word 0x%x)", v);
     return QGEMM_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- the no-allocation variant
+namespace {
+
+// Scratch for qgemm_run_noalloc: one fixed array in every device that loads the library.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QGEMM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(QGEMM_ERR_UNSUPPORTED, "device %d beyond the supported %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the scratch array");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return QGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                      const float* T, void* C, int c_dtype, void* stream) {
+    // the same checks qgemm_run makes, so the size test below sees a valid shape
+    int blk = block;
+    int rc = check_shape(K, N, mode, &blk);
+    if (rc != QGEMM_OK) return rc;
+    if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
+    if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
+        return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
+    if (M == 0 || N == 0) return QGEMM_OK;
+    const size_t need = run_ws(M, K, N, mode, blk, a_dtype);
+    if (need > QGEMM_NOALLOC_SCRATCH_BYTES)
+        return fail(QGEMM_ERR_WORKSPACE, "this call needs %zu bytes of scratch; the built-in scratch holds %u", need,
+                    QGEMM_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != QGEMM_OK) return rc;
+    return qgemm_run(M, K, N, mode, block, A, a_dtype, Bp, T, C, c_dtype, scratch, QGEMM_NOALLOC_SCRATCH_BYTES,
+                     stream);
 }
 
 const char* qgemm_error_string(int code) {
