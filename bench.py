@@ -62,25 +62,38 @@ def bound_of(w: synth.Workload) -> str:
     return "hbm" if w.M <= 16 else "tensor"
 
 
-def src_hash() -> str:
+# source files of each workload's dominant kernel: a recorded DRAM-traffic figure is used only
+# while these files are unchanged since the capture
+KERNEL_SOURCES = {
+    "decode": ["decode_kernel.cuh", "decode_int4.cu", "decode_int8.cu", "decode_float.cu", "internal.h"],
+    "prefill": ["prefill.cu", "internal.h"],
+}
+
+
+def kernel_of(w: synth.Workload) -> str:
+    return "decode" if (w.M <= 16 and w.mode != synth.MODE_W4A8 and w.a_dtype != synth.F32) else "prefill"
+
+
+def src_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_quantized_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:12]
 
 
-def measured_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+def measured_traffic(w: synth.Workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.txt: workload kernel source-hash bytes), if it was taken on this source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = src_hash()
+    kern = kernel_of(w)
+    cur = src_hash(kern)
     for ln in open(path):
         parts = ln.split()
-        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == workload and parts[2] == cur:
+        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == w.name and parts[1] == kern and parts[2] == cur:
             return int(float(parts[3]))
     return None
 
@@ -362,6 +375,7 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--print-src-hash", action="store_true", help="print the dominant kernel's source hash and exit")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="pack, run this many plain calls of the layer, print a status line and exit "
                          "(a small fixed command to run under a profiler; no timing)")
@@ -373,6 +387,9 @@ def main():
         import dataclasses
         w = dataclasses.replace(w, M=args.m)
 
+    if args.print_src_hash:
+        print(kernel_of(w), src_hash(kernel_of(w)))
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     peaks = load_peaks()
@@ -431,7 +448,8 @@ def main():
         else (w.flops / (r["ms_plain"] / 1e3 / args.steps) / 1e12 * world),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-                     "traffic": measured_traffic(w.name), "algorithmic_bytes": alg},
+                     "traffic": measured_traffic(w), "algorithmic_bytes": alg,
+                     "kernel": kernel_of(w)},
         "clocks": r["clocks"], "gpu_launches": args.steps * r["launches_per_call"],
         "e2e": {"value": (alg / r["e2e_s"] / 1e9) if bound == "hbm" else (w.flops / r["e2e_s"] / 1e12),
                 "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "ms_per_step": r["e2e_s"] * 1e3,
