@@ -2,8 +2,11 @@
 //
 // Benchmark page "MNN GemmSpeed 基准测试实战", «测试用例与注册机制»: the W4A8 path quantizes the
 // activations dynamically to INT8. Per row, in float32: as = max|a| / 127, qa = clamp(rint(a / as),
-// -127, 127) with ties to even (qa = 0 when as == 0), rowsum = sum qa. The division is the
-// correctly rounded IEEE one, so the codes match any IEEE float32 evaluation bit for bit.
+// -127, 127) with ties to even (qa = 0 when as == 0), rowsum = sum qa. The codes equal those of
+// the correctly rounded IEEE quotient bit for bit. The quotient itself is not needed, only the
+// integer it rounds to, so each element first uses y = a * RN(1 / as): for |a / as| <= 127 it is
+// within 2.3e-5 of RN(a / as), hence rounds to the same integer unless it lies within 3e-5 of a
+// half-integer; only those rare elements take the exact division.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -62,6 +65,7 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rcp = s != 0.f ? __frcp_rn(s) : 0.f;
 
     int sum = 0;
     for (int k = threadIdx.x * 8; k < K; k += kThreads * 8) {
@@ -73,7 +77,10 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
         for (int j = 0; j < 8; ++j) {
             int c = 0;
             if (s != 0.f) {
-                c = __float2int_rn(__fdiv_rn(v[j], s));
+                float y = v[j] * rcp;
+                const float f = fabsf(y - rintf(y));   // distance to the nearest integer, <= 0.5
+                if (f > 0.49997f) y = __fdiv_rn(v[j], s);   // near a half-integer: decide exactly
+                c = __float2int_rn(y);
                 c = c < -127 ? -127 : (c > 127 ? 127 : c);
             }
             sum += c;
