@@ -31,7 +31,11 @@
  *         INT4 / W4A8  uint8 [N][K/2], byte j of a row = q[2j] | q[2j+1] << 4
  *         INT8         uint8 [N][K]
  *         FLOAT        [N][K] in the activation dtype (f16, bf16 or f32)
- *   T   float32 [N][K/block][2] = {offset, scale} per (channel, block); absent in FLOAT mode
+ *   T   float32 {offset, scale} per (channel n, block b), absent in FLOAT mode, stored in groups
+ *       of 16 channels: [ceil(N/16)][K/block][16][2], i.e. the pair of (n, b) at pair index
+ *       ((n / 16) * (K/block) + b) * 16 + n % 16; channels N .. ceil(N/16)*16 - 1 hold zeros.
+ *       (The page keeps oc x blockNum pairs; the grouping lets one 16-channel unit's pairs for
+ *       a K-range be one contiguous copy.)
  *   A   [M][K] in a_dtype;  C  [M][N] in c_dtype
  * Dequantization: w[k][n] = q[n][k] * scale[n][k/block] + offset[n][k/block], with unsigned
  * codes q in [0, 15] (4-bit) or [0, 255] (8-bit).
@@ -74,8 +78,9 @@ extern "C" {
  * quantized modes ignore w_dtype. Returns 0 for invalid arguments. */
 size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype);
 
-/* Bytes of the {offset, scale} table T (0 in FLOAT mode or for invalid arguments).
- * block = 0 means one block over all of K. */
+/* Bytes of the {offset, scale} table T, including the zero channels that complete the last
+ * group of 16 (0 in FLOAT mode or for invalid arguments). block = 0 means one block over all
+ * of K. */
 size_t qgemm_table_bytes(int K, int N, int mode, int block);
 
 /* Bytes of scratch device memory qgemm_run needs for this call (0 if none). The decode
@@ -173,7 +178,8 @@ int qgemm_get_option(int option);
 /* ---------------------------------------------------------------- status */
 
 /* Synchronize `stream`, then report (and clear) the library's device status word: QGEMM_OK,
- * QGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait, or QGEMM_ERR_CUDA. */
+ * QGEMM_ERR_TIMEOUT if a kernel gave up a bounded wait, or QGEMM_ERR_CUDA on a CUDA error or if
+ * a kernel found its shared memory misaligned for its TMA copies (it then skipped its work). */
 int qgemm_status(void* stream);
 
 /* Static name of a status code. */

@@ -18,6 +18,15 @@ MANT_BITS = {0: 23, 1: 10, 2: 7}       # by output dtype
 MIN_EXP = {0: -126, 1: -14, 2: -126}
 
 
+def table_rows(T_flat, N: int, nb: int) -> np.ndarray:
+    """The library's {offset, scale} table, stored in 16-channel groups [ceil(N/16)][nb][16][2],
+    as [N][nb][2]; asserts that the padding channels of the last group are zero."""
+    G = (N + 15) // 16
+    t = np.asarray(T_flat).reshape(G, nb, 16, 2).transpose(0, 2, 1, 3).reshape(G * 16, nb, 2)
+    assert not t[N:].any(), "padding channels of the table are not zero"
+    return t[:N]
+
+
 def half_ulp(R: np.ndarray, c_dtype: int) -> np.ndarray:
     a = np.abs(R)
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))

@@ -30,6 +30,7 @@ def test_exports_every_declared_symbol():
 def test_sizes():
     assert qg.qgemm_packed_bytes(4096, 11008, qg.MODE_INT4) == 4096 * 11008 // 2
     assert qg.qgemm_table_bytes(4096, 11008, qg.MODE_INT4, 64) == 11008 * 64 * 8
+    assert qg.qgemm_table_bytes(256, 200, qg.MODE_INT4, 64) == 208 * 4 * 8    # channels padded to 16
     assert qg.qgemm_packed_bytes(4096, 4096, qg.MODE_INT8) == 4096 * 4096
     assert qg.qgemm_table_bytes(4096, 4096, qg.MODE_INT8, 0) == 4096 * 8
     assert qg.qgemm_packed_bytes(256, 512, qg.MODE_FLOAT, qg.F16) == 256 * 512 * 2

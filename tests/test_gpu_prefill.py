@@ -8,7 +8,7 @@ import torch
 import oracle
 import weight_quantized_gemm_gb300 as qg
 from weight_quantized_gemm_gb300 import synth
-from tests._util import check_close, ensure_built, to_numpy_values, torch_dtype, torch_from
+from tests._util import check_close, ensure_built, table_rows, to_numpy_values, torch_dtype, torch_from
 from tests.test_gpu_decode import gpu_pack, gpu_run, layer_case
 
 pytestmark = pytest.mark.gpu
@@ -43,7 +43,7 @@ def _sampled_case(w: synth.Workload, npts: int = 4096, seed: int = 0):
     q, T = oracle.quantize(W_np, blk, oracle.QMAX[w.mode])
     Bp, Tg = gpu_pack(W_np, w.mode, w.block)
     assert np.array_equal(Bp.cpu().numpy().reshape(w.N, -1), oracle.pack(q, oracle.NBITS[w.mode]))
-    assert np.array_equal(Tg.cpu().numpy().reshape(T.shape), T)
+    assert np.array_equal(table_rows(Tg.cpu().numpy(), w.N, T.shape[1]), T)
     got = gpu_run(w.M, w.K, w.N, w.mode, w.block, A_np, w.a_dtype, Bp, Tg, w.c_dtype)
     rng = np.random.default_rng(seed)
     mi = rng.integers(0, w.M, npts)

@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs p) {
         float s = 1.f, o = 0.f;
         if constexpr (FMT != FMT_FLOAT) {
             const int blk = k0 / p.block;
-            o = p.T[((size_t)n * nb + blk) * 2 + 0];
-            s = p.T[((size_t)n * nb + blk) * 2 + 1];
+            o = p.T[tab_index(n, nb, blk) * 2 + 0];
+            s = p.T[tab_index(n, nb, blk) * 2 + 1];
         }
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {

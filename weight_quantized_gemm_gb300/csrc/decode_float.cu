@@ -1,10 +1,14 @@
-// Tensor-core decode kernel instantiations for float weights (see decode_kernel.cuh).
-#include "decode_kernel.cuh"
+// Decode kernel instantiations for float weights: the TMA-fed kernel (decode_stream.cuh) where the
+// shape suits it, else the cp.async kernel (decode_kernel.cuh).
+#include "decode_stream.cuh"
 
 namespace qg {
 
 cudaError_t launch_decode_float(const DecodeArgs& a, cudaStream_t s) {
-    return a.a_dtype == DT_BF16 ? dec::launch_fmt<FMT_FLOAT, true>(a, s) : dec::launch_fmt<FMT_FLOAT, false>(a, s);
+    const bool bf = a.a_dtype == DT_BF16;
+    if (dstream::supported<FMT_FLOAT>(a))
+        return bf ? dstream::launch_fmt<FMT_FLOAT, true>(a, s) : dstream::launch_fmt<FMT_FLOAT, false>(a, s);
+    return bf ? dec::launch_fmt<FMT_FLOAT, true>(a, s) : dec::launch_fmt<FMT_FLOAT, false>(a, s);
 }
 
 }  // namespace qg

@@ -1,10 +1,14 @@
-// Tensor-core decode kernel instantiations for int4 weights (see decode_kernel.cuh).
-#include "decode_kernel.cuh"
+// Decode kernel instantiations for int4 weights: the TMA-fed kernel (decode_stream.cuh) where the
+// shape suits it, else the cp.async kernel (decode_kernel.cuh).
+#include "decode_stream.cuh"
 
 namespace qg {
 
 cudaError_t launch_decode_int4(const DecodeArgs& a, cudaStream_t s) {
-    return a.a_dtype == DT_BF16 ? dec::launch_fmt<FMT_INT4, true>(a, s) : dec::launch_fmt<FMT_INT4, false>(a, s);
+    const bool bf = a.a_dtype == DT_BF16;
+    if (dstream::supported<FMT_INT4>(a))
+        return bf ? dstream::launch_fmt<FMT_INT4, true>(a, s) : dstream::launch_fmt<FMT_INT4, false>(a, s);
+    return bf ? dec::launch_fmt<FMT_INT4, true>(a, s) : dec::launch_fmt<FMT_INT4, false>(a, s);
 }
 
 }  // namespace qg

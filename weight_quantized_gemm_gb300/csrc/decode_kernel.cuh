@@ -289,7 +289,6 @@ struct Issuer {
     int sb0;               // global index of the warp's first sub-block
     int sb_per_blk;        // sub-blocks per table block
     unsigned valid;        // bit j: the warp's sub-block j lies inside the K-range
-    bool tab16;            // a pair's two table entries are one aligned 16-byte copy
     uint32_t wdst0, wdst1; // this lane's weight destinations inside a stage (rows g, g + 8)
     uint32_t tdst;         // this lane's table destination inside a stage (4-byte copies)
     int trow;              // the table row this lane copies (4-byte copies)
@@ -322,15 +321,10 @@ struct Issuer {
                     const int q = R::kGroups == 2 ? (lane >> 4) : 0;
                     if (q == jp) {
                         const int rr = lane & 15;
-                        const float* src = T + ((size_t)min(n0 + rr, N - 1) * nb + blk(2 * jp)) * 2;
+                        const float* src = T + tab_index(n0 + rr, nb, blk(2 * jp)) * 2;
                         const uint32_t dst = sg + 1024 + rr * 16;
-                        if (tab16 && ok(2 * jp + 1)) {
-                            cp_async16(dst, src);
-                        } else {
-                            cp_async8(dst, src);
-                            if (ok(2 * jp + 1))
-                                cp_async8(dst + 8, src + 2 * (blk(2 * jp + 1) - blk(2 * jp)));
-                        }
+                        cp_async8(dst, src);
+                        if (ok(2 * jp + 1)) cp_async8(dst + 8, src + 32 * (blk(2 * jp + 1) - blk(2 * jp)));
                     }
                 }
             }
@@ -351,12 +345,12 @@ struct Issuer {
                     cp_async16(sj + wdst1 + 512, w1 + o + 16);
                 }
                 if constexpr (kScaled)
-                    cp_async4(sj + 32 * R::kLaneBytes + tdst, T + ((size_t)rt * nb + blk(j)) * 2 + (lane & 1));
+                    cp_async4(sj + 32 * R::kLaneBytes + tdst, T + tab_index(rt, nb, blk(j)) * 2 + (lane & 1));
             }
         }
         if constexpr (PERCH && FMT != FMT_FLOAT) {
             const int rt = min(n0 + trow, N - 1);
-            cp_async4(st + R::kGroups * R::kGroupBytes + tdst, T + (size_t)rt * 2 + (lane & 1));
+            cp_async4(st + R::kGroups * R::kGroupBytes + tdst, T + tab_index(rt, 1, 0) * 2 + (lane & 1));
         }
     }
 };
@@ -407,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
     issue.nb = nb;
     issue.g = g;
     issue.lane = lane;
-    issue.tab16 = sb_per_blk == 1 && (nb & 1) == 0 && (sb_begin & 1) == 0;
     if constexpr (R::kPair) {
         issue.wdst0 = (uint32_t)(g * 64 + ((t ^ (g & 3)) << 4));
         issue.wdst1 = issue.wdst0 + 512;
@@ -720,6 +713,8 @@ cudaError_t launch_c(const DecodeArgs& a, cudaStream_t s) {
     }
 }
 
+// Shapes the TMA-fed kernel of decode_stream.cuh does not take: 9 <= M <= 16, or packed rows that
+// are not a multiple of 128 bytes.
 template <int FMT, bool BF>
 cudaError_t launch_fmt(const DecodeArgs& a, cudaStream_t s) {
     const bool perch = FMT != FMT_FLOAT && a.block == a.K;

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (qgemm_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -11,6 +12,16 @@ enum Fmt { FMT_FLOAT = 0, FMT_INT4 = 1, FMT_INT8 = 2 };
 enum Dt { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 inline size_t dt_size(int dt) { return dt == DT_F32 ? 4 : 2; }
+
+// The {offset, scale} table T holds one float32 pair per (output channel n, K-block b), stored in
+// groups of 16 channels: [ceil(N / 16)][nb][16][2]. The entries of a 16-channel group for a run
+// of K-blocks are then one contiguous, 128-byte aligned range (one bulk copy), and the 16
+// channels of one K-block are 128 contiguous bytes. Channels past N (up to the next multiple of
+// 16) hold zeros. tab_index gives the pair's index (in pairs).
+__host__ __device__ __forceinline__ size_t tab_index(int n, int nb, int b) {
+    return (((size_t)(n >> 4) * nb + b) << 4) + (n & 15);
+}
+inline size_t table_pairs(int N, int nb) { return (size_t)((N + 15) / 16) * 16 * nb; }
 
 // SM count the grid heuristics are sized for (GB300: 152 SMs). A constant, so that host-side
 // size queries (workspace bytes) give the same answer with or without a GPU present.
@@ -77,5 +88,14 @@ int option_overlap();
 
 // device status word (bounded waits that gave up); read and cleared by qgemm_status
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+// Device address of the status word on the current device (nullptr if it cannot be had), for
+// kernels compiled in other translation units.
+unsigned int* status_word_address();
+
+// cuTensorMapEncodeTiled, taken from the driver once (nullptr if the driver lacks it)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 }  // namespace qg

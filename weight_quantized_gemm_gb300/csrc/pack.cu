@@ -52,9 +52,9 @@ __global__ void __launch_bounds__(256) quant_pack_kernel(const float* __restrict
     }
     // 2) scale and offset
     const float scale = __fdiv_rn(__fsub_rn(hi, lo), (float)kQmax);
-    if (ty == 0 && n < N) {
-        T[((size_t)n * nb + b) * 2 + 0] = lo;
-        T[((size_t)n * nb + b) * 2 + 1] = scale;
+    if (ty == 0 && n < (N + 15) / 16 * 16) {   // channels past N fill their 16-channel group with zeros
+        T[tab_index(n, nb, b) * 2 + 0] = n < N ? lo : 0.f;
+        T[tab_index(n, nb, b) * 2 + 1] = n < N ? scale : 0.f;
     }
     // 3) codes, a K-chunk at a time, then packed rows written along K
     constexpr int kBytesPerRow = kChunk * NBITS / 8;       // 32 or 64

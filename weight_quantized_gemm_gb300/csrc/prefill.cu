@@ -23,10 +23,12 @@
 // an abort flag, all roles leave their loops, in-flight work is drained (bounded) and TMEM is
 // freed before the kernel returns.
 #include <cuda.h>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace qg {
 
@@ -42,11 +44,10 @@ constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple 
 constexpr int kStageBytesX = kMaxBN * kBK * 2;
 constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
 constexpr int kThreads = kWarps * 32;
+constexpr int kEpiThreads = (kWarps - 2) * 32;   // dequant + epilogue threads
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;            // accumulator columns [0, BN)
 constexpr int kACol = 256;            // A stages from column 256: 32 columns each (64 with a low part)
-constexpr long long kWaitCycles = 2000000000LL;   // ~1 s at GB300 clocks
-constexpr unsigned kStatusTimeout = 1u;
 
 enum Wf { WF_INT4 = 0, WF_INT8 = 1, WF_FLOAT = 2, WF_CODES4 = 3 };
 enum Epi { EPI_STORE = 0, EPI_W4A8 = 1, EPI_ACC = 2 };
@@ -62,52 +63,13 @@ struct Params {
 };
 
 // ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Waits for the phase of `parity` to complete; gives up after ~1 s or when another role has
-// aborted. Returns false if it gave up (and then raises the abort flag).
+using ptx::mbar_arrive;
+using ptx::mbar_expect_tx;
+using ptx::mbar_init;
+using ptx::smem_u32;
+using ptx::tma_load_2d;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCycles) {
-                *abort_flag = 1;
-                atomicOr(&g_status_word, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
+    return ptx::mbar_wait(bar, parity, abort_flag, &g_status_word);
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -350,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_a)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w)) : "memory");
+        ptx::prefetch_tmap(&tmap_a);
+        ptx::prefetch_tmap(&tmap_w);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -429,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if constexpr (kTable) {
                     if (ks < nk)
                         return __ldg(reinterpret_cast<const float2*>(
-                            p.T + ((size_t)rc * p.nb + (ks * kBK + 32 * h) / p.block) * 2));
+                            p.T + tab_index(rc, p.nb, (ks * kBK + 32 * h) / p.block) * 2));
                 }
                 return make_float2(0.f, 1.f);
             };
@@ -460,13 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (lane == 0) mbar_arrive(full_a(s));
             }
         }
-        // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2)
+        // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
+        // The tile is written transposed into the (now idle) stage buffers as [m][128 n] and then
+        // copied out row by row with 16-byte stores.
         const bool ok = mbar_wait(acc_full, 0u, abort_flag) && !*abort_flag;
         tc_fence_after();
+        constexpr int kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2;
+        uint8_t* tile = smem;
         if (ok) {
             float ws = 0.f, wo = 0.f;
             if constexpr (EPI == EPI_W4A8) {
-                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + (size_t)rc * 2));
+                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
                 wo = t.x;
                 ws = t.y;
             }
@@ -474,24 +440,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kAccCol + c0, v);
                 tmem_ld_wait();
-                if (row < p.N) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int m = m_tile + c0 + i;
-                        if (m < p.M) {
-                            const float d = __uint_as_float(v[i]);
-                            const size_t idx = (size_t)m * p.N + row;
-                            if constexpr (EPI == EPI_ACC) {
-                                p.acc[idx] = __float2int_rn(d);
-                            } else if constexpr (EPI == EPI_W4A8) {
-                                // d is the exact integer accumulator (see the file comment)
-                                const float rs = (float)__ldg(p.rowsum + m);
-                                store_c<CDT>(p.C, idx, __ldg(p.a_scale + m) * fmaf(ws, d, wo * rs));
-                            } else {
-                                store_c<CDT>(p.C, idx, d);
-                            }
-                        }
+                for (int i = 0; i < 32; ++i) {
+                    const int ml = c0 + i;
+                    const float d = __uint_as_float(v[i]);
+                    const size_t t = (size_t)ml * kBM + r;
+                    if constexpr (EPI == EPI_ACC) {
+                        reinterpret_cast<int32_t*>(tile)[t] = __float2int_rn(d);
+                    } else if constexpr (EPI == EPI_W4A8) {
+                        // d is the exact integer accumulator (see the file comment)
+                        const int m = min(m_tile + ml, p.M - 1);
+                        store_c<CDT>(tile, t, __ldg(p.a_scale + m) * fmaf(ws, d, wo * (float)__ldg(p.rowsum + m)));
+                    } else {
+                        store_c<CDT>(tile, t, d);
                     }
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
+        if (ok) {
+            const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
+            constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
+            constexpr int kChunks = kBM / kPer;               // chunks per tile row
+            uint8_t* out = EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C);
+            const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+            for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
+                const int ml = idx / kChunks, c = idx - ml * kChunks;
+                const int n0 = c * kPer;
+                if (n0 >= nvalid) continue;
+                const uint8_t* src = tile + ((size_t)ml * kBM + n0) * kEsz;
+                uint8_t* dst = out + ((size_t)(m_tile + ml) * p.N + n_tile + n0) * kEsz;
+                if (vec && n0 + kPer <= nvalid) {
+                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+                } else {
+                    for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
+                        for (int b = 0; b < kEsz; ++b) dst[e * kEsz + b] = src[e * kEsz + b];
                 }
             }
         }
@@ -511,25 +494,9 @@ __global__ void codes_to_f16_kernel(const int8_t* __restrict__ qa, __half* __res
 }
 
 // ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
 // [M][K] 16-bit activations, box of 64 (K) x BN (rows), 128-byte swizzle; rows past M read 0.
 cudaError_t make_tmap(CUtensorMap* map, const void* A, bool bf16, int M, int K, int BN) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -552,7 +519,7 @@ size_t smem_bytes() { return (size_t)kStages * kStageBytes + 256; }
 // The packed weight rows [N][row bytes] as a 2-D byte (quantized formats) or 16-bit (float mode,
 // 128-byte swizzle) tensor; box = one stage of 128 rows; rows past N read 0.
 cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N, int K) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUresult r;
     if (wf == WF_FLOAT) {
@@ -597,6 +564,36 @@ cudaError_t launch_cdt(const CUtensorMap& amap, const CUtensorMap& wmap, const P
 }
 
 }  // namespace pf
+
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+unsigned int* g_status_addr[kMaxDevices] = {};
+}  // namespace
+
+unsigned int* status_word_address() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_status_addr[dev];
+}
 
 cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
     unsigned int h = 0;

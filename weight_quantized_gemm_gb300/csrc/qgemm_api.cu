@@ -105,7 +105,7 @@ size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype) {
 
 size_t qgemm_table_bytes(int K, int N, int mode, int block) {
     if (check_shape(K, N, mode, &block) != QGEMM_OK || mode == QGEMM_MODE_FLOAT) return 0;
-    return (size_t)N * (K / block) * 2 * sizeof(float);
+    return qg::table_pairs(N, K / block) * 2 * sizeof(float);
 }
 
 size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype) {
@@ -236,7 +236,8 @@ int qgemm_status(void* stream) {
     int v = 0;
     e = qg::read_and_clear_status(&v, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (v != 0) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status word 0x%x)", v);
+    if (v & 1) return fail(QGEMM_ERR_TIMEOUT, "a kernel gave up a bounded wait (status word 0x%x)", v);
+    if (v != 0) return fail(QGEMM_ERR_CUDA, "a kernel found its shared memory misaligned and did no work (status word 0x%x)", v);
     return QGEMM_OK;
 }
 
