@@ -65,8 +65,9 @@ def bound_of(w: synth.Workload) -> str:
 # source files of each workload's dominant kernel: a recorded DRAM-traffic figure is used only
 # while these files are unchanged since the capture
 KERNEL_SOURCES = {
-    "decode": ["decode_kernel.cuh", "decode_int4.cu", "decode_int8.cu", "decode_float.cu", "internal.h"],
-    "prefill": ["prefill.cu", "internal.h"],
+    "decode": ["decode_stream.cuh", "decode_kernel.cuh", "decode_int4.cu", "decode_int8.cu", "decode_float.cu",
+               "ptx.cuh", "internal.h"],
+    "prefill": ["prefill.cu", "ptx.cuh", "internal.h"],
 }
 
 
