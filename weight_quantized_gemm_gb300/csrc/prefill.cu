@@ -39,7 +39,6 @@ namespace pf {
 
 constexpr int kBM = 128;              // output channels per tile (MMA M)
 constexpr int kBK = 64;               // K per pipeline stage
-constexpr int kStages = 4;
 constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
 constexpr int kStageBytesX = kMaxBN * kBK * 2;
 constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
@@ -101,6 +100,11 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdes
 __device__ __forceinline__ uint4 lds128u(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
     return v;
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -272,20 +276,46 @@ __device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
 // 16-bit weights [128 rows][128 B] with the 128-byte swizzle in float mode (then read by the
 // MMA directly as its A operand).
 constexpr int kWOff = kStageBytesX;
-constexpr int kWBytesMax = kBM * kBK * 2;
-constexpr int kStageBytes = kStageBytesX + kWBytesMax;
+constexpr size_t kSmemMax = 232448;   // opt-in shared memory per block
 template <int WF>
 struct WBox {
     static constexpr int kRowBytes = (WF == WF_INT4 || WF == WF_CODES4) ? kBK / 2 : (WF == WF_INT8 ? kBK : 2 * kBK);
 };
+// Ring depth per format: a stage is the activation box plus only the weight bytes the format
+// needs (4 KB for 4-bit codes, 8 KB for 8-bit, 16 KB for 16-bit weights), as many stages as
+// shared memory holds (6, 5, 4), and no more than the TMEM columns left for A stages beside the
+// accumulator allow (8 stages of 32 columns, 4 of 64 with the bf16 hi/lo split). The deeper ring
+// covers the TMA latency plus the dequantization of a stage, which only starts once its weights
+// have landed.
+struct Maps {                 // the kernel's tensor maps
+    CUtensorMap a;            // activations
+    CUtensorMap w;            // packed weights
+    CUtensorMap t;            // grouped {offset, scale} table (formats with a table)
+};
+// The {offset, scale} entries of a stage's K-block for the tile's 128 channels (8 groups of 16,
+// 128 bytes each in the grouped table layout) follow the weight box: one more TMA box.
+template <int WF>
+struct TBox {
+    static constexpr bool kOn = WF == WF_INT4 || WF == WF_INT8;
+    static constexpr int kOff = kWOff + kBM * WBox<WF>::kRowBytes;
+    static constexpr int kBytes = kOn ? kBM * 8 : 0;
+};
+template <int WF, bool BF>
+struct Ring {
+    static constexpr int kStageBytes = kStageBytesX + kBM * WBox<WF>::kRowBytes + TBox<WF>::kBytes;   // multiples of 1024
+    static constexpr int kSmemStages = (int)((kSmemMax - 256) / kStageBytes);
+    static constexpr int kTmemStages = (kTmemCols - kACol) / Split<WF, BF>::kStageCols;
+    static constexpr int kStages = kSmemStages < kTmemStages ? kSmemStages : kTmemStages;
+    static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256;
+};
 
 // One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), all of K.
 template <int WF, bool BF, int EPI, int CDT>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                                                              const __grid_constant__ CUtensorMap tmap_w, Params p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Maps maps, Params p) {
     constexpr bool kDequant = WF != WF_FLOAT;          // weights go through the dequant warps into TMEM
     constexpr bool kTable = WF == WF_INT4 || WF == WF_INT8;
     constexpr int kCols = Split<WF, BF>::kStageCols;
+    constexpr int kStages = Ring<WF, BF>::kStages, kStageBytes = Ring<WF, BF>::kStageBytes;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BN = p.BN;
@@ -312,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        ptx::prefetch_tmap(&tmap_a);
-        ptx::prefetch_tmap(&tmap_w);
+        ptx::prefetch_tmap(&maps.a);
+        ptx::prefetch_tmap(&maps.w);
+        if constexpr (TBox<WF>::kOn) ptx::prefetch_tmap(&maps.t);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -325,19 +356,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---------------- TMA producer: the A slice and the weight slice of each stage
+        // ---------------- TMA producer: the A slice, the weight slice and (formats with a table)
+        // the stage's {offset, scale} entries of each stage
         if (lane == 0) {
-            const uint32_t bytes = (uint32_t)BN * kBK * 2 + (uint32_t)kBM * WBox<WF>::kRowBytes;
-            int issued = 0;
+            const uint32_t bytes =
+                (uint32_t)BN * kBK * 2 + (uint32_t)kBM * WBox<WF>::kRowBytes + (uint32_t)TBox<WF>::kBytes;
+            const int spb = p.block / kBK;   // stages per table block (the block is a multiple of 64)
+            int issued = 0, tb = 0, tc = 0;  // table block of stage ks, and ks's position in it
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
                 mbar_expect_tx(full_x(s), bytes);
-                tma_load_2d(st_s + s * kStageBytes, &tmap_a, ks * kBK, m_tile, full_x(s));
+                tma_load_2d(st_s + s * kStageBytes, &maps.a, ks * kBK, m_tile, full_x(s));
                 // weight box: x in bytes for the packed formats, in elements for float mode
-                tma_load_2d(st_s + s * kStageBytes + kWOff, &tmap_w,
+                tma_load_2d(st_s + s * kStageBytes + kWOff, &maps.w,
                             WF == WF_FLOAT ? ks * kBK : ks * WBox<WF>::kRowBytes, n_tile, full_x(s));
+                if constexpr (TBox<WF>::kOn) {
+                    // 8 groups of 16 channels, block tb: x = 32 floats per block, y = group
+                    tma_load_2d(st_s + s * kStageBytes + TBox<WF>::kOff, &maps.t, 32 * tb, n_tile / 16, full_x(s));
+                    if (++tc == spb) {
+                        tc = 0;
+                        ++tb;
+                    }
+                }
                 issued = ks + 1;
             }
             if (*abort_flag) {   // let the copies already issued land before the block exits
@@ -385,18 +427,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int rc = row < p.N ? row : p.N - 1;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         if constexpr (kDequant) {
-            // {offset, scale} of the stages ks .. ks + 3, shifted along as the stages advance
-            float2 tq[4];
-            auto table = [&](int ks) {
-                if constexpr (kTable) {
-                    if (ks < nk)
-                        return __ldg(reinterpret_cast<const float2*>(
-                            p.T + tab_index(rc, p.nb, (ks * kBK + 32 * h) / p.block) * 2));
-                }
-                return make_float2(0.f, 1.f);
-            };
-#pragma unroll
-            for (int i = 0; i < 4; ++i) tq[i] = table(i);
             for (int ks = 0; ks < nk; ++ks) {
                 const int s = ks % kStages;
                 const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
@@ -406,12 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 uint4 raw[4];
                 raw[0] = lds128u(wsrc);
                 if constexpr (WF == WF_INT8) raw[1] = lds128u(wsrc + 16);
+                float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and stage
+                if constexpr (TBox<WF>::kOn) e = lds64f(st_s + s * kStageBytes + TBox<WF>::kOff + r * 8);
                 uint32_t out[16], rest[16];
-                convert32<WF, BF>(raw, tq[0].y, tq[0].x, out, rest);
-                tq[0] = tq[1];
-                tq[1] = tq[2];
-                tq[2] = tq[3];
-                tq[3] = table(ks + 4);
+                convert32<WF, BF>(raw, e.y, e.x, out, rest);
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 tmem_st16(tmem + lane_base + kACol + s * kCols + 16 * h, out);
@@ -514,7 +542,6 @@ int pick_bn(int M) {
     return (M + 63) / 64 * 64;
 }
 
-size_t smem_bytes() { return (size_t)kStages * kStageBytes + 256; }
 
 // The packed weight rows [N][row bytes] as a 2-D byte (quantized formats) or 16-bit (float mode,
 // 128-byte swizzle) tensor; box = one stage of 128 rows; rows past N read 0.
@@ -544,22 +571,39 @@ cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The grouped {offset, scale} table [ceil(N/16)][nb][16][2] as a 2-D float tensor: x = 32 floats
+// per K-block of a group (16 channels x 2), y = group (stride nb * 128 bytes); box = one K-block
+// of 8 groups (the tile's 128 channels); groups past the end read 0.
+cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)32 * nb, (cuuint64_t)((N + 15) / 16)};
+    const cuuint64_t strides[1] = {(cuuint64_t)nb * 128};
+    const cuuint32_t box[2] = {32, (cuuint32_t)(kBM / 16)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(T), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int WF, bool BF, int EPI, int CDT>
-cudaError_t launch_k(const CUtensorMap& amap, const CUtensorMap& wmap, const Params& p, cudaStream_t s) {
+cudaError_t launch_k(const Maps& maps, const Params& p, cudaStream_t s) {
     auto kern = prefill_kernel<WF, BF, EPI, CDT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes());
+    constexpr size_t smem = Ring<WF, BF>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN);
-    kern<<<grid, kThreads, smem_bytes(), s>>>(amap, wmap, p);
+    kern<<<grid, kThreads, smem, s>>>(maps, p);
     return cudaGetLastError();
 }
 
 template <int WF, bool BF, int EPI>
-cudaError_t launch_cdt(const CUtensorMap& amap, const CUtensorMap& wmap, const Params& p, int c_dtype, cudaStream_t s) {
+cudaError_t launch_cdt(const Maps& maps, const Params& p, int c_dtype, cudaStream_t s) {
     switch (c_dtype) {
-        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(amap, wmap, p, s);
-        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(amap, wmap, p, s);
-        default: return launch_k<WF, BF, EPI, DT_BF16>(amap, wmap, p, s);
+        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(maps, p, s);
+        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(maps, p, s);
+        default: return launch_k<WF, BF, EPI, DT_BF16>(maps, p, s);
     }
 }
 
@@ -622,18 +666,20 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     const bool bf = a.a_dtype == DT_BF16;
     const int wf = a.fmt == FMT_INT4 ? pf::WF_INT4 : (a.fmt == FMT_INT8 ? pf::WF_INT8 : pf::WF_FLOAT);
-    CUtensorMap amap, wmap;
-    cudaError_t e = pf::make_tmap(&amap, a.A, bf, a.M, a.K, p.BN);
-    if (e == cudaSuccess) e = pf::make_wmap(&wmap, a.Bp, wf, bf, a.N, a.K);
+    pf::Maps maps;
+    cudaError_t e = pf::make_tmap(&maps.a, a.A, bf, a.M, a.K, p.BN);
+    if (e == cudaSuccess) e = pf::make_wmap(&maps.w, a.Bp, wf, bf, a.N, a.K);
+    if (e == cudaSuccess) e = wf == pf::WF_FLOAT ? cudaSuccess : pf::make_table_map(&maps.t, a.T, a.N, p.nb);
     if (e != cudaSuccess) return e;
+    if (wf == pf::WF_FLOAT) maps.t = maps.w;   // unused
     if (a.fmt == FMT_INT4)
-        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
+        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
     if (a.fmt == FMT_INT8)
-        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
-    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s)
-              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(amap, wmap, p, a.c_dtype, s);
+        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
+                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
+    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
+              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
 }
 
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
@@ -642,12 +688,13 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc;
-    CUtensorMap amap, wmap;
-    cudaError_t e = pf::make_tmap(&amap, a.qa16, false, a.M, a.K, p.BN);
-    if (e == cudaSuccess) e = pf::make_wmap(&wmap, a.Bp, pf::WF_CODES4, false, a.N, a.K);
+    pf::Maps maps;
+    cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
+    if (e == cudaSuccess) e = pf::make_wmap(&maps.w, a.Bp, pf::WF_CODES4, false, a.N, a.K);
     if (e != cudaSuccess) return e;
-    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(amap, wmap, p, s);
-    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(amap, wmap, p, a.c_dtype, s);
+    maps.t = maps.w;   // unused: the per-channel scale is applied in the epilogue
+    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(maps, p, s);
+    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s) {
