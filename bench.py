@@ -220,6 +220,21 @@ def run_reference(args, w: synth.Workload) -> dict:
 
 
 # ---------------------------------------------------------------- the GPU arm
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The timed region as the slowest rank saw it; every rank gets the same value."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_step: float, step_s: float, world: int) -> float:
+    """Whole-job throughput: every rank runs the same per-step work (replicas, weak scaling)."""
+    return units_per_step / step_s * world
+
+
 def to_torch(arr: np.ndarray, code: int, device):
     import torch
     if code == synth.BF16:
@@ -306,12 +321,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        ms = start.elapsed_time(end)
-        if dist is not None:
-            t = torch.tensor([ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(start.elapsed_time(end), dist, device)
 
     ms_plain = timed(graphs[0])
     with ClockSampler(device.index if device.index is not None else 0) as clk:
@@ -426,8 +436,8 @@ def main():
     r = run_gpu(args, w, rank, world, dist)
     step_s = r["ms"] / 1e3 / args.steps
     alg = algorithmic_bytes(w)
-    gbs = alg / step_s / 1e9 * world
-    tflops = w.flops / step_s / 1e12 * world
+    gbs = job_rate(alg, step_s, world) / 1e9
+    tflops = job_rate(w.flops, step_s, world) / 1e12
     bound = bound_of(w)
     if bound == "hbm":
         achieved, peak, unit = alg / step_s / 1e9, peaks["hbm_gbs"], "GB/s"
@@ -445,8 +455,8 @@ def main():
                        launch_overlap="QGEMM_OPT_LAUNCH_OVERLAP=1 (programmatic dependent launch)"),
         "tflops": tflops, "gbs": gbs,
         "ms_per_step_no_overlap": r["ms_plain"] / args.steps,
-        "value_no_overlap": (alg / (r["ms_plain"] / 1e3 / args.steps) / 1e9 * world) if bound == "hbm"
-        else (w.flops / (r["ms_plain"] / 1e3 / args.steps) / 1e12 * world),
+        "value_no_overlap": (job_rate(alg, r["ms_plain"] / 1e3 / args.steps, world) / 1e9) if bound == "hbm"
+        else (job_rate(w.flops, r["ms_plain"] / 1e3 / args.steps, world) / 1e12),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "traffic": measured_traffic(w), "algorithmic_bytes": alg,
