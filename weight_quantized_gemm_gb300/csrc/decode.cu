@@ -4,7 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "decode_kernel.cuh"
+#include "decode_stream.cuh"
 
 namespace qg {
 
@@ -113,12 +113,13 @@ cudaError_t launch_f32_a(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int decode_splits(int M, int K, int N) {
-    // K-range per thread block: at most 4 (M <= 8) or 2 (M > 8) sub-blocks per warp, so that the
-    // activations fit in registers or shared memory; split further while the units alone cannot
-    // give every SM a thread block, keeping at least one sub-block per warp.
+int decode_splits(int M, int K, int N, int fmt, int block) {
+    // K-range per thread block: 64 sub-blocks for the TMA-fed kernel (and the cp.async kernel at
+    // M <= 8), 32 for the cp.async kernel at 9 <= M <= 16, so that the activations fit in
+    // registers or shared memory; split further while the units alone cannot give every SM a
+    // thread block, keeping at least one sub-block per warp.
     const int nsb = K / 64;
-    const int sb_max = M <= 8 ? Share<1>::kSbMaxNt : Share<2>::kSbMaxNt;
+    const int sb_max = (dstream::stream_takes(M, K, fmt, block) || M <= 8) ? Share<1>::kSbMaxNt : Share<2>::kSbMaxNt;
     int splits = (nsb + sb_max - 1) / sb_max;
     const int groups = (N + 15) / 16;
     while (groups * splits < kTargetSms && nsb / (splits * 2) >= dec::kWarps) splits *= 2;
@@ -139,7 +140,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
         c.M = a.M - m0 < 16 ? a.M - m0 : 16;
         c.A = static_cast<const uint8_t*>(a.A) + (size_t)m0 * a.K * esz;
         c.C = static_cast<uint8_t*>(a.C) + (size_t)m0 * a.N * csz;
-        c.splits = decode_splits(c.M, a.K, a.N);
+        c.splits = decode_splits(c.M, a.K, a.N, a.fmt, a.block);
         cudaError_t e = launch_one(c, s);
         if (e != cudaSuccess || c.splits <= 1) {
             if (e != cudaSuccess) return e;

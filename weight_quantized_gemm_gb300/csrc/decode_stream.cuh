@@ -51,12 +51,24 @@ constexpr int kRows = 16;                            // output channels per unit
 constexpr int kSliceBytes = 128;
 constexpr int kSliceTile = kRows * kSliceBytes;      // one slice of a unit in shared memory (2 KB)
 constexpr int kWStage = kCWarps * kSliceTile;        // weight region of a stage (32 KB)
-constexpr int kRed = 4;                              // units per reduction round
-constexpr int kRedBytes = kRed * kCWarps * 32 * 16;  // one float4 per lane, warp and unit
 constexpr int kMaxDepth = 6;
 constexpr size_t kMaxSmem = 232448;                  // opt-in shared memory per block (sm_100 class)
 constexpr unsigned kStatusMisaligned = 2u;          // status bit: shared memory not 1024-byte aligned
-constexpr int kFixedBytes = kRedBytes + kCWarps * 8 * 4 + 2 * kMaxDepth * 8 + 16;
+constexpr int kNJ = 4;                               // sub-blocks per consumer warp and unit (64 per unit)
+
+// Shared memory besides the ring, for NT column tiles of 8 rows of A. One tile (M <= 8) keeps the
+// B fragments in registers and reduces 4 units at a time. Two tiles (9 <= M <= 16) would need
+// 64 fragment registers per thread, so the fragments of the warp's 4 sub-blocks x 2 tiles go to
+// shared memory (1 KB per sub-block and tile, as two 16-byte planes per lane so that reads are
+// conflict-free, plus the 8 column sums), and partial sums are reduced after every unit.
+template <int NT>
+struct Budget {
+    static constexpr int kRed = NT == 1 ? 4 : 1;                           // units per reduction round
+    static constexpr int kRedBytes = kRed * kCWarps * NT * 32 * 16;       // a float4 per lane, tile, warp, unit
+    static constexpr int kFragBytes = NT == 1 ? 0 : kCWarps * kNJ * NT * 1024;
+    static constexpr int kSumBytes = NT == 1 ? 0 : kCWarps * kNJ * NT * 32;
+    static constexpr int kFixedBytes = kRedBytes + kCWarps * NT * 32 + kFragBytes + kSumBytes + 2 * kMaxDepth * 8 + 16;
+};
 
 template <int FMT>
 struct Geo {
@@ -93,10 +105,14 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
 }
 
-template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL>
+template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL, int NT>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ CUtensorMap wmap, Params p) {
     using G = Geo<FMT>;
-    constexpr int SPS = G::kSps, CH = G::kChunks, NJ = SPS * CH;
+    using Bu = Budget<NT>;
+    constexpr int SPS = G::kSps, CH = G::kChunks, NJ = kNJ, kRed = Bu::kRed;
+    static_assert(SPS * CH == kNJ, "64 sub-blocks per unit over 16 warps");
+    static_assert(NT == 1 || !ONECOL, "one column is one tile");
+    constexpr bool kRegB = NT == 1;   // B fragments in registers
     constexpr bool kTable = FMT != FMT_FLOAT;
     constexpr bool kScaled = kTable && !PERCH;   // scale per sub-block
     constexpr float kBias = Codes<FMT, BF>::kBias;
@@ -112,9 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int nu = (int)blockIdx.x < groups ? (groups - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
     const int n_step = (int)gridDim.x * kRows;
 
-    float* red = reinterpret_cast<float*>(smem + (size_t)p.depth * p.stage_bytes);
-    float* wsum = red + kRedBytes / 4;                                   // [warp][8] column sums
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wsum + kCWarps * 8);   // full[kMaxDepth] | empty[kMaxDepth]
+    float* red = reinterpret_cast<float*>(smem + (size_t)p.depth * p.stage_bytes);   // [unit][warp][tile][lane] float4
+    float* wsum = red + Bu::kRedBytes / 4;                                            // [warp][tile][8] column sums
+    uint8_t* fragp = reinterpret_cast<uint8_t*>(wsum + kCWarps * NT * 8);   // [warp][jj][tile][plane][lane] 16 B
+    float2* fsum = reinterpret_cast<float2*>(fragp + Bu::kFragBytes);       // [warp][jj][tile][t] column sums
+    uint64_t* bars = reinterpret_cast<uint64_t*>(fragp + Bu::kFragBytes + Bu::kSumBytes);   // full | empty
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxDepth);
     const uint32_t s_base = smem_u32(smem);
     auto full = [&](int s) { return smem_u32(bars + s); };
@@ -194,23 +212,45 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const uint16_t* A = static_cast<const uint16_t*>(p.A);
     // the warp's sub-block jj = c * SPS + j (stage c of a unit): global index
     // (sl_begin + c * bz + warp) * SPS + j; B operand fragments and column sums in registers
-    uint32_t breg[NJ][8];
-    float2 sreg[NJ];
+    uint32_t breg[kRegB ? NJ : 1][8];
+    float2 sreg[kRegB ? NJ : 1];
     uint32_t toff[NJ];   // byte offset of the sub-block's entry (16 rows x 8 bytes) in a stage's table
+    float2 stot[NT];     // PERCH: column sums over the split's whole K-range, per tile
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) stot[nt] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int jj = 0; jj < NJ; ++jj) {
         const int c = jj / SPS, j = jj % SPS;
         const int sb = (sl_begin + c * p.bz + warp) * SPS + j;
         const bool valid = c < chunks && warp < p.bz && sb < sb_end;
-        uint32_t nw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (valid && g < p.M) {
-            const uint4* src = reinterpret_cast<const uint4*>(A + (size_t)g * p.K + (size_t)sb * 64 + t * 16);
-            const uint4 x = src[0], y = src[1];
-            nw[0] = x.x; nw[1] = x.y; nw[2] = x.z; nw[3] = x.w;
-            nw[4] = y.x; nw[5] = y.y; nw[6] = y.z; nw[7] = y.w;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int m = nt * 8 + g;   // the row of A this lane's fragment column holds
+            uint32_t nw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (valid && m < p.M) {
+                const uint4* src = reinterpret_cast<const uint4*>(A + (size_t)m * p.K + (size_t)sb * 64 + t * 16);
+                const uint4 x = src[0], y = src[1];
+                nw[0] = x.x; nw[1] = x.y; nw[2] = x.z; nw[3] = x.w;
+                nw[4] = y.x; nw[5] = y.y; nw[6] = y.z; nw[7] = y.w;
+            }
+            uint32_t bt[8];
+            b_frags<FMT>(nw, bt);
+            const float2 S = col_sums<BF>(bt);
+            if constexpr (kRegB) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) breg[jj][q] = bt[q];
+                sreg[jj] = S;
+            } else {
+                uint4* plane = reinterpret_cast<uint4*>(fragp + (size_t)((warp * NJ + jj) * NT + nt) * 1024);
+                plane[lane] = make_uint4(bt[0], bt[1], bt[2], bt[3]);
+                plane[32 + lane] = make_uint4(bt[4], bt[5], bt[6], bt[7]);
+                if (g == 0) fsum[((warp * NJ + jj) * NT + nt) * 4 + t] = S;
+            }
+            if constexpr (PERCH) {
+                stot[nt].x += S.x;
+                stot[nt].y += S.y;
+            }
         }
-        b_frags<FMT>(nw, breg[jj]);
-        sreg[jj] = col_sums<BF>(breg[jj]);
         toff[jj] = 0;
         if constexpr (kTable) {
             const int sb_c0 = (sl_begin + c * p.bz) * SPS;
@@ -218,25 +258,28 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             toff[jj] = (uint32_t)((sbv / p.sb_per_blk - sb_c0 / p.sb_per_blk) * 128);
         }
     }
-    float2 stot = make_float2(0.f, 0.f);   // PERCH: column sums over the split's whole K-range
+    if constexpr (!kRegB) __syncwarp();   // a warp reads only its own fragments
     if constexpr (PERCH) {
-#pragma unroll
-        for (int jj = 0; jj < NJ; ++jj) {
-            stot.x += sreg[jj].x;
-            stot.y += sreg[jj].y;
-        }
         if (g == 0) {
-            wsum[warp * 8 + 2 * t] = stot.x;
-            wsum[warp * 8 + 2 * t + 1] = stot.y;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                wsum[(warp * NT + nt) * 8 + 2 * t] = stot[nt].x;
+                wsum[(warp * NT + nt) * 8 + 2 * t + 1] = stot[nt].y;
+            }
         }
         consumer_sync();
-        stot = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kCWarps; ++w) {
-            stot.x += wsum[w * 8 + 2 * t];
-            stot.y += wsum[w * 8 + 2 * t + 1];
+        for (int nt = 0; nt < NT; ++nt) {
+            stot[nt] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kCWarps; ++w) {
+                stot[nt].x += wsum[(w * NT + nt) * 8 + 2 * t];
+                stot[nt].y += wsum[(w * NT + nt) * 8 + 2 * t + 1];
+            }
         }
     }
+    const uint32_t frag_s = smem_u32(fragp) + (uint32_t)(warp * NJ * NT * 1024 + lane * 16);
+    const uint32_t fsum_s = smem_u32(fsum) + (uint32_t)(warp * NJ * NT * 32 + t * 8);
 
     // per-lane read offset inside the warp's slice of a stage: row g, the 16-byte chunk holding
     // the lane's 16 k of sub-block 0 (bytes 8t (Int4), 16t (Int8) or 32t (16-bit) of it), chunk
@@ -255,7 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     for (int ui0 = 0; ui0 < nu; ui0 += kRed) {
         const int nr = min(kRed, nu - ui0);
         for (int r = 0; r < nr; ++r) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f}, dp[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[NT][4], dp[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[nt][q] = dp[nt][q] = 0.f;
             float2 tp0 = make_float2(0.f, 0.f), tp1 = tp0;   // PERCH: {offset, scale} of rows g, g + 8
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
@@ -307,33 +354,47 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
                             a[0][1] = y0.x; a[0][3] = y0.y; a[1][1] = y0.z; a[1][3] = y0.w;
                             a[2][1] = y1.x; a[2][3] = y1.y; a[3][1] = y1.z; a[3][3] = y1.w;
                         }
-                        const uint32_t* b = breg[jj];
+                        float2 e0 = make_float2(0.f, 0.f), e1 = e0;   // {o, s} of rows g, g + 8
                         if constexpr (kScaled) {
-                            const float2 e0 = lds64f(ts + trow0 + toff[jj]);   // {o, s} of row g
-                            const float2 e1 = lds64f(ts + trow1 + toff[jj]);   // row g + 8
-                            mma16816_zc<BF>(dp, a[0][0], a[0][1], a[0][2], a[0][3], b[0], b[1]);
+                            e0 = lds64f(ts + trow0 + toff[jj]);
+                            e1 = lds64f(ts + trow1 + toff[jj]);
+                        }
 #pragma unroll
-                            for (int q = 1; q < 4; ++q)
-                                mma16816<BF>(dp, a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
-                            const float o0 = fmaf(-kBias, e0.y, e0.x), o1 = fmaf(-kBias, e1.y, e1.x);
-                            const float2 S = sreg[jj];
-                            // dp[0], dp[1]: channel row g, columns 2t, 2t + 1; dp[2], dp[3]: row g + 8
-                            acc[0] = fmaf(o0, S.x, fmaf(e0.y, dp[0], acc[0]));
-                            acc[2] = fmaf(o1, S.x, fmaf(e1.y, dp[2], acc[2]));
-                            if constexpr (!ONECOL) {
-                                acc[1] = fmaf(o0, S.y, fmaf(e0.y, dp[1], acc[1]));
-                                acc[3] = fmaf(o1, S.y, fmaf(e1.y, dp[3], acc[3]));
+                        for (int nt = 0; nt < NT; ++nt) {
+                            uint32_t b[8];
+                            float2 S;
+                            if constexpr (kRegB) {
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) b[q] = breg[jj][q];
+                                S = sreg[jj];
+                            } else {
+                                const uint32_t fa = frag_s + (uint32_t)((jj * NT + nt) * 1024);
+                                const uint4 b0 = lds128(fa), b1 = lds128(fa + 512);
+                                b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                                b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                                S = lds64f(fsum_s + (uint32_t)((jj * NT + nt) * 32));
                             }
-                        } else {
-                            // one accumulation for the unit: per-channel scale (applied at the
-                            // unit's end) or no scale at all (16-bit weights)
-                            auto mma4 = [&](float(&d)[4]) {
+                            if constexpr (kScaled) {
+                                mma16816_zc<BF>(dp[nt], a[0][0], a[0][1], a[0][2], a[0][3], b[0], b[1]);
+#pragma unroll
+                                for (int q = 1; q < 4; ++q)
+                                    mma16816<BF>(dp[nt], a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
+                                const float o0 = fmaf(-kBias, e0.y, e0.x), o1 = fmaf(-kBias, e1.y, e1.x);
+                                // dp[0], dp[1]: channel row g, columns 2t, 2t + 1; dp[2], dp[3]: row g + 8
+                                acc[nt][0] = fmaf(o0, S.x, fmaf(e0.y, dp[nt][0], acc[nt][0]));
+                                acc[nt][2] = fmaf(o1, S.x, fmaf(e1.y, dp[nt][2], acc[nt][2]));
+                                if constexpr (!ONECOL) {
+                                    acc[nt][1] = fmaf(o0, S.y, fmaf(e0.y, dp[nt][1], acc[nt][1]));
+                                    acc[nt][3] = fmaf(o1, S.y, fmaf(e1.y, dp[nt][3], acc[nt][3]));
+                                }
+                            } else {
+                                // one accumulation for the unit: per-channel scale (applied at the
+                                // unit's end) or no scale at all (16-bit weights)
+                                float(&d)[4] = PERCH ? dp[nt] : acc[nt];
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
                                     mma16816<BF>(d, a[q][0], a[q][1], a[q][2], a[q][3], b[2 * q], b[2 * q + 1]);
-                            };
-                            if constexpr (PERCH) mma4(dp);
-                            else mma4(acc);
+                            }
                         }
                     }
                 }
@@ -344,29 +405,31 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
                     ph ^= 1u;
                 }
             }
-            if constexpr (PERCH) {
-                // the offset term o' * sum_k a belongs to the unit once: warp 0 adds it
-                const float o0 = warp == 0 ? fmaf(-kBias, tp0.y, tp0.x) : 0.f;
-                const float o1 = warp == 0 ? fmaf(-kBias, tp1.y, tp1.x) : 0.f;
-                acc[0] = fmaf(o0, stot.x, tp0.y * dp[0]);
-                acc[1] = fmaf(o0, stot.y, tp0.y * dp[1]);
-                acc[2] = fmaf(o1, stot.x, tp1.y * dp[2]);
-                acc[3] = fmaf(o1, stot.y, tp1.y * dp[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if constexpr (PERCH) {
+                    // the offset term o' * sum_k a belongs to the unit once: warp 0 adds it
+                    const float o0 = warp == 0 ? fmaf(-kBias, tp0.y, tp0.x) : 0.f;
+                    const float o1 = warp == 0 ? fmaf(-kBias, tp1.y, tp1.x) : 0.f;
+                    acc[nt][0] = fmaf(o0, stot[nt].x, tp0.y * dp[nt][0]);
+                    acc[nt][1] = fmaf(o0, stot[nt].y, tp0.y * dp[nt][1]);
+                    acc[nt][2] = fmaf(o1, stot[nt].x, tp1.y * dp[nt][2]);
+                    acc[nt][3] = fmaf(o1, stot[nt].y, tp1.y * dp[nt][3]);
+                }
+                *reinterpret_cast<float4*>(red + (((size_t)(r * kCWarps + warp) * NT + nt) * 32 + lane) * 4) =
+                    make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
             }
-            *reinterpret_cast<float4*>(red + ((size_t)(r * kCWarps + warp) * 32 + lane) * 4) =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         // fixed-order sum of the 16 warps' partials of the round's units
         consumer_sync();
-        {
-            const int idx = threadIdx.x;   // 0 .. 511: (unit r, lane ln, element cc)
-            const int r = idx >> 7, ln = (idx >> 2) & 31, cc = idx & 3;
+        for (int idx = threadIdx.x; idx < kRed * NT * 128; idx += kCWarps * 32) {   // (unit r, tile nt, lane ln, element cc)
+            const int r = idx / (NT * 128), nt = (idx / 128) % NT, ln = (idx >> 2) & 31, cc = idx & 3;
             const int row = (int)blockIdx.x * kRows + (ui0 + r) * n_step + (ln >> 2) + (cc >= 2 ? 8 : 0);
-            const int m = 2 * (ln & 3) + (cc & 1);
+            const int m = nt * 8 + 2 * (ln & 3) + (cc & 1);
             if (r < nr && row < p.N && m < p.M && ok) {
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kCWarps; ++w) sum += red[((size_t)(r * kCWarps + w) * 32 + ln) * 4 + cc];
+                for (int w = 0; w < kCWarps; ++w) sum += red[(((size_t)(r * kCWarps + w) * NT + nt) * 32 + ln) * 4 + cc];
                 if (gridDim.y > 1)
                     p.partial[((size_t)blockIdx.y * p.M + m) * p.N + row] = sum;
                 else
@@ -383,8 +446,38 @@ struct Plan {
     size_t smem;
 };
 
+// Packed bytes per 64-wide sub-block of a row.
+inline int sb_bytes(int fmt) { return fmt == FMT_INT4 ? 32 : (fmt == FMT_INT8 ? 64 : 128); }
+
+// Bytes of one ring stage: the weight box plus the table entries a stage can need.
+inline int stage_bytes_for(int fmt, int K, int block) {
+    int table = 0;
+    if (fmt != FMT_FLOAT) {
+        const int sps = kSliceBytes / sb_bytes(fmt), spb = block / 64, nb = K / block;
+        const int ent_bound = (kCWarps * sps - 1) / spb + 2;
+        table = 128 * (nb < ent_bound ? nb : ent_bound);
+    }
+    return (kWStage + table + 1023) / 1024 * 1024;
+}
+
+// Ring depth that fits beside the fixed shared memory of NT column tiles (0 if fewer than 2).
+template <int NT>
+inline int ring_depth(int fmt, int K, int block) {
+    const int d = (int)((kMaxSmem - Budget<NT>::kFixedBytes) / (size_t)stage_bytes_for(fmt, K, block));
+    return d < 2 ? 0 : (d < kMaxDepth ? d : kMaxDepth);
+}
+
+// True if this kernel takes the shape: at most 16 rows of A, packed rows a multiple of 128 bytes,
+// and (for two column tiles) at least two ring stages beside the fragments. Shapes it takes run
+// with at most 64 sub-blocks per thread block (the split-K rule in decode.cu uses this).
+inline bool stream_takes(int M, int K, int fmt, int block) {
+    if (M < 1 || M > 16 || ((long long)(K / 64) * sb_bytes(fmt)) % kSliceBytes != 0) return false;
+    return M <= 8 ? ring_depth<1>(fmt, K, block) > 0 : ring_depth<2>(fmt, K, block) > 0;
+}
+
+
 // Ring geometry for a launch with `splits` K-splits; false if the shape does not fit.
-template <int FMT>
+template <int FMT, int NT>
 bool make_plan(const DecodeArgs& a, Plan* out) {
     using G = Geo<FMT>;
     Params& p = out->p;
@@ -398,18 +491,12 @@ bool make_plan(const DecodeArgs& a, Plan* out) {
     p.bz = sl_split < kCWarps ? sl_split : kCWarps;
     p.chunks = (sl_split + p.bz - 1) / p.bz;
     if (p.chunks > G::kChunks) return false;
-    int table = 0;   // bytes: at most this many entries of 16 rows x 8 bytes per stage
-    if (FMT != FMT_FLOAT) {
-        const int ent_bound = (kCWarps * G::kSps - 1) / p.sb_per_blk + 2;
-        table = 128 * (p.nb < ent_bound ? p.nb : ent_bound);
-    }
     p.row_bytes = p.nsb * G::kSbBytes;
     if (p.row_bytes % kSliceBytes != 0) return false;
-    p.stage_bytes = (kWStage + table + 1023) / 1024 * 1024;
-    const int depth = (int)((kMaxSmem - kFixedBytes) / (size_t)p.stage_bytes);
-    p.depth = depth < kMaxDepth ? depth : kMaxDepth;
+    p.stage_bytes = stage_bytes_for(FMT, a.K, a.block);
+    p.depth = ring_depth<NT>(FMT, a.K, a.block);
     if (p.depth < 2) return false;
-    out->smem = (size_t)p.depth * p.stage_bytes + kFixedBytes;
+    out->smem = (size_t)p.depth * p.stage_bytes + Budget<NT>::kFixedBytes;
     return true;
 }
 
@@ -428,16 +515,15 @@ inline cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int row_bytes, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// True if the shape suits this kernel: at most 8 rows of A and packed rows a multiple of 128 bytes.
 template <int FMT>
 inline bool supported(const DecodeArgs& a) {
-    return a.M <= 8 && ((long long)(a.K / 64) * Geo<FMT>::kSbBytes) % kSliceBytes == 0;
+    return stream_takes(a.M, a.K, FMT, a.block);
 }
 
-template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL>
+template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL, int NT>
 cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     Plan plan;
-    if (!make_plan<FMT>(a, &plan)) return cudaErrorInvalidValue;
+    if (!make_plan<FMT, NT>(a, &plan)) return cudaErrorInvalidValue;
     plan.p.A = a.A;
     plan.p.Bp = static_cast<const uint8_t*>(a.Bp);
     plan.p.T = a.T;
@@ -448,7 +534,7 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     CUtensorMap wmap;
     cudaError_t e = make_wmap(&wmap, a.Bp, plan.p.row_bytes, a.N, plan.p.bz);
     if (e != cudaSuccess) return e;
-    auto kern = stream_kernel<FMT, BF, PERCH, CDT, ONECOL>;
+    auto kern = stream_kernel<FMT, BF, PERCH, CDT, ONECOL, NT>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return e;
     const int groups = (a.N + kRows - 1) / kRows;
@@ -467,21 +553,23 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, wmap, plan.p);
 }
 
-template <int FMT, bool BF, bool PERCH, bool ONECOL>
+template <int FMT, bool BF, bool PERCH, bool ONECOL, int NT>
 cudaError_t launch_c(const DecodeArgs& a, cudaStream_t s) {
     switch (a.splits > 1 ? DT_F32 : a.c_dtype) {
-        case DT_F32: return launch_v<FMT, BF, PERCH, DT_F32, ONECOL>(a, s);
-        case DT_F16: return launch_v<FMT, BF, PERCH, DT_F16, ONECOL>(a, s);
-        default: return launch_v<FMT, BF, PERCH, DT_BF16, ONECOL>(a, s);
+        case DT_F32: return launch_v<FMT, BF, PERCH, DT_F32, ONECOL, NT>(a, s);
+        case DT_F16: return launch_v<FMT, BF, PERCH, DT_F16, ONECOL, NT>(a, s);
+        default: return launch_v<FMT, BF, PERCH, DT_BF16, ONECOL, NT>(a, s);
     }
 }
 
-// M <= 8
+// Shapes stream_takes accepts (M <= 16)
 template <int FMT, bool BF>
 cudaError_t launch_fmt(const DecodeArgs& a, cudaStream_t s) {
-    const bool perch = FMT != FMT_FLOAT && a.block == a.K;
-    if (a.M == 1) return perch ? launch_c<FMT, BF, FMT != FMT_FLOAT, true>(a, s) : launch_c<FMT, BF, false, true>(a, s);
-    return perch ? launch_c<FMT, BF, FMT != FMT_FLOAT, false>(a, s) : launch_c<FMT, BF, false, false>(a, s);
+    constexpr bool kPerch = FMT != FMT_FLOAT;   // the per-channel specialization exists for tabled formats
+    const bool perch = kPerch && a.block == a.K;
+    if (a.M == 1) return perch ? launch_c<FMT, BF, kPerch, true, 1>(a, s) : launch_c<FMT, BF, false, true, 1>(a, s);
+    if (a.M <= 8) return perch ? launch_c<FMT, BF, kPerch, false, 1>(a, s) : launch_c<FMT, BF, false, false, 1>(a, s);
+    return perch ? launch_c<FMT, BF, kPerch, false, 2>(a, s) : launch_c<FMT, BF, false, false, 2>(a, s);
 }
 
 }  // namespace dstream

@@ -47,8 +47,9 @@ struct DecodeArgs {
     int splits;       // number of K-splits across thread blocks (>= 1)
     int overlap;      // launch with a programmatic dependency on the previous kernel
 };
-// K-splits the decode kernel uses for this shape (1 = none).
-int decode_splits(int M, int K, int N);
+// K-splits the decode kernels use for this shape, at most 16 rows of A (1 = none); block is the
+// table's K-group (K for per-channel).
+int decode_splits(int M, int K, int N, int fmt, int block);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 // Exact float32 CUDA-core kernel (any activation dtype, any M); used for f32 activations.
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);

@@ -72,9 +72,9 @@ size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype) {
     if (choose_path(M, K, N, mode, a_dtype) != PATH_DECODE) return 0;
     // the decode kernel runs 16 rows of A at a time; split-K partials are per 16-row launch
     const int mc = M < 16 ? M : 16;
-    const int splits = qg::decode_splits(mc, K, N);
+    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
+    const int splits = qg::decode_splits(mc, K, N, fmt, block == 0 ? K : block);
     return splits > 1 ? (size_t)splits * mc * N * sizeof(float) : 0;
-    (void)block;
 }
 
 }  // namespace
