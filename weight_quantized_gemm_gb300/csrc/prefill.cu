@@ -59,6 +59,7 @@ struct Params {
     const float* a_scale;     // W4A8: per-row activation scale
     const int32_t* rowsum;    // W4A8: per-row sum of activation codes
     int32_t* acc;             // EPI_ACC output
+    int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -291,6 +292,7 @@ struct Maps {                 // the kernel's tensor maps
     CUtensorMap a;            // activations
     CUtensorMap w;            // packed weights
     CUtensorMap t;            // grouped {offset, scale} table (formats with a table)
+    CUtensorMap c;            // the output, when Params::c_tma (stored by TMA from the staged tile)
 };
 // The {offset, scale} entries of a stage's K-block for the tile's 128 channels (8 groups of 16,
 // 128 bytes each in the grouped table layout) follow the weight box: one more TMA box.
@@ -303,10 +305,10 @@ struct TBox {
 template <int WF, bool BF>
 struct Ring {
     static constexpr int kStageBytes = kStageBytesX + kBM * WBox<WF>::kRowBytes + TBox<WF>::kBytes;   // multiples of 1024
-    static constexpr int kSmemStages = (int)((kSmemMax - 256) / kStageBytes);
+    static constexpr int kSmemStages = (int)((kSmemMax - 256 - kMaxBN * 8) / kStageBytes);
     static constexpr int kTmemStages = (kTmemCols - kACol) / Split<WF, BF>::kStageCols;
     static constexpr int kStages = kSmemStages < kTmemStages ? kSmemStages : kTmemStages;
-    static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256;
+    static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + kMaxBN * 8;   // + W4A8 row factors
 };
 
 // One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), all of K.
@@ -327,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     //       empty[kStages] (MMAs of the stage done) | acc_full
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
+    float2* rowf = reinterpret_cast<float2*>(smem + kStages * kStageBytes + 256);
     const uint32_t st_s = smem_u32(smem);
     auto full_x = [&](int s) { return smem_u32(bars + s); };
     auto full_a = [&](int s) { return smem_u32(bars + kStages + s); };
@@ -420,6 +424,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
         }
     } else {
+        if constexpr (EPI == EPI_W4A8) {
+            // the row factors, once per tile, while the first stages are in flight
+            for (int i = threadIdx.x - 64; i < BN; i += kEpiThreads) {
+                const int m = min(m_tile + i, p.M - 1);
+                const float as = __ldg(p.a_scale + m);
+                rowf[i] = make_float2(as, as * (float)__ldg(p.rowsum + m));
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
+        }
         // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each stage
         const int q = warp & 3, h = (warp - 2) >> 2;
         const int r = 32 * q + lane;                 // row inside the tile
@@ -476,15 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     if constexpr (EPI == EPI_ACC) {
                         reinterpret_cast<int32_t*>(tile)[t] = __float2int_rn(d);
                     } else if constexpr (EPI == EPI_W4A8) {
-                        // d is the exact integer accumulator (see the file comment)
-                        const int m = min(m_tile + ml, p.M - 1);
-                        store_c<CDT>(tile, t, __ldg(p.a_scale + m) * fmaf(ws, d, wo * (float)__ldg(p.rowsum + m)));
+                        // d is the exact integer accumulator (see the file comment):
+                        // as * (ws * d + wo * rowsum) = ws * (as * d) + wo * (as * rowsum)
+                        const float2 f = rowf[ml];   // the same row for the whole warp: a broadcast
+                        store_c<CDT>(tile, t, fmaf(ws, f.x * d, wo * f.y));
                     } else {
                         store_c<CDT>(tile, t, d);
                     }
                 }
             }
         }
+        if (p.c_tma) {
+            // one TMA store of the staged tile (rows and channels past the end are not written);
+            // the block may retire once the store has read shared memory
+            ptx::fence_proxy_async_smem();
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
+            if (ok && threadIdx.x == 64) {
+                ptx::tma_store_2d(&maps.c, n_tile, m_tile, smem_u32(tile));
+                ptx::bulk_commit();
+                ptx::bulk_wait_read();
+            }
+        } else {
         asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
         if (ok) {
             const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
@@ -505,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         for (int b = 0; b < kEsz; ++b) dst[e * kEsz + b] = src[e * kEsz + b];
                 }
             }
+        }
         }
     }
     tc_fence_before();
@@ -585,6 +611,25 @@ cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb) {
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The output [M][N] (bf16 / f16 / f32, or int32 accumulators) as a 2-D tensor; box = one tile of
+// 128 channels x BN rows, matching the staged [rows][128] tile. Only when a row is a whole number
+// of 16-byte units (TMA strides) and the base is 16-byte aligned; else returns false.
+bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN) {
+    const size_t esz = kind == DT_F32 || kind < 0 ? 4 : 2;
+    if (((size_t)N * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return false;
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const CUtensorMapDataType dt = kind < 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                   : (kind == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (kind == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16));
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * esz};
+    const cuuint32_t box[2] = {(cuuint32_t)kBM, (cuuint32_t)BN};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int WF, bool BF, int EPI, int CDT>
@@ -672,6 +717,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     if (e == cudaSuccess) e = wf == pf::WF_FLOAT ? cudaSuccess : pf::make_table_map(&maps.t, a.T, a.N, p.nb);
     if (e != cudaSuccess) return e;
     if (wf == pf::WF_FLOAT) maps.t = maps.w;   // unused
+    p.c_tma = pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN) ? 1 : 0;
+    if (!p.c_tma) maps.c = maps.a;             // unused
     if (a.fmt == FMT_INT4)
         return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
                   : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
@@ -693,6 +740,9 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     if (e == cudaSuccess) e = pf::make_wmap(&maps.w, a.Bp, pf::WF_CODES4, false, a.N, a.K);
     if (e != cudaSuccess) return e;
     maps.t = maps.w;   // unused: the per-channel scale is applied in the epilogue
+    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN) ? 1 : 0)
+                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN) ? 1 : 0);
+    if (!p.c_tma) maps.c = maps.a;     // unused
     if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(maps, p, s);
     return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
 }
