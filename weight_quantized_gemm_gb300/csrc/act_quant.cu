@@ -40,22 +40,71 @@ __device__ __forceinline__ void load8(const void* A, size_t i, float (&v)[8]) {
     }
 }
 
+// The codes of 8 values: RN-even of v * RN(1/s) unless one of them lies within 3e-5 of a
+// half-integer, then of the correctly rounded quotient for all 8; clamped to +-127 (as rounded
+// floats, exact); the f16 copies, the int8 bytes and the running sum of the codes.
+__device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rcp, int& sum, uint4& h16, uint2& q8) {
+    float r[8];
+    float dev = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float y = v[j] * rcp;
+        r[j] = rintf(y);
+        dev = fmaxf(dev, fabsf(y - r[j]));   // distance to the nearest integer, <= 0.5
+    }
+    if (dev > 0.49997f) {   // near a half-integer: decide by the exact quotient
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[j] = rintf(__fdiv_rn(v[j], s));
+    }
+    uint32_t hw[4];
+    float cs = 0.f;   // the chunk's code sum, exact (|cs| <= 1016)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        r[j] = fminf(fmaxf(r[j], -127.f), 127.f);
+        cs += r[j];
+    }
+    sum += __float2int_rn(cs);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __half2 h = __floats2half2_rn(r[2 * j], r[2 * j + 1]);   // integers <= 127: exact
+        hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    h16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    uint32_t b[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j >> 2] |= ((uint32_t)__float2int_rn(r[j]) & 0xFFu) << (8 * (j & 3));
+    q8 = make_uint2(b[0], b[1]);
+}
+
+// One block per row. The row is read once: each thread keeps up to kCache chunks of 8 values in
+// registers between the max pass and the quantize pass (K <= 8192); longer rows re-read the rest.
 template <int ADT>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* __restrict__ A,
                                                              int8_t* __restrict__ qa, __half* __restrict__ qa16,
                                                              float* __restrict__ as, int32_t* __restrict__ rowsum) {
+    constexpr int kCache = 4;
     __shared__ float s_max[kThreads / 32];
     __shared__ int s_sum[kThreads / 32];
     const int m = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t row = (size_t)m * K;
 
+    float v[kCache][8];
     float amax = 0.f;
-    for (int k = threadIdx.x * 8; k < K; k += kThreads * 8) {
-        float v[8];
-        load8<ADT>(A, row + k, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    for (int i = 0; i < kCache; ++i) {
+        const int k = (threadIdx.x + i * kThreads) * 8;
+        if (k < K) {
+            load8<ADT>(A, row + k, v[i]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+        }
+    }
+    for (int k = (threadIdx.x + kCache * kThreads) * 8; k < K; k += kThreads * 8) {
+        float w[8];
+        load8<ADT>(A, row + k, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(w[j]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -65,30 +114,25 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
     const float s = __fdiv_rn(amax, 127.0f);
-    const float rcp = s != 0.f ? __frcp_rn(s) : 0.f;
+    const float rcp = s != 0.f ? __frcp_rn(s) : 0.f;   // s == 0: every code is 0
 
     int sum = 0;
-    for (int k = threadIdx.x * 8; k < K; k += kThreads * 8) {
-        float v[8];
-        load8<ADT>(A, row + k, v);
-        uint32_t packed[2] = {0u, 0u};
-        __half h[8];
+    auto emit = [&](int k, const float (&w)[8]) {
+        uint4 h16;
+        uint2 q8;
+        quantize8(w, s, rcp, sum, h16, q8);
+        if (qa16) *reinterpret_cast<uint4*>(qa16 + row + k) = h16;
+        if (qa) *reinterpret_cast<uint2*>(qa + row + k) = q8;
+    };
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            int c = 0;
-            if (s != 0.f) {
-                float y = v[j] * rcp;
-                const float f = fabsf(y - rintf(y));   // distance to the nearest integer, <= 0.5
-                if (f > 0.49997f) y = __fdiv_rn(v[j], s);   // near a half-integer: decide exactly
-                c = __float2int_rn(y);
-                c = c < -127 ? -127 : (c > 127 ? 127 : c);
-            }
-            sum += c;
-            packed[j >> 2] |= (uint32_t)(c & 0xFF) << (8 * (j & 3));
-            h[j] = __int2half_rn(c);   // |c| <= 127: exact
-        }
-        if (qa) *reinterpret_cast<uint2*>(qa + row + k) = make_uint2(packed[0], packed[1]);
-        if (qa16) *reinterpret_cast<uint4*>(qa16 + row + k) = *reinterpret_cast<const uint4*>(h);
+    for (int i = 0; i < kCache; ++i) {
+        const int k = (threadIdx.x + i * kThreads) * 8;
+        if (k < K) emit(k, v[i]);
+    }
+    for (int k = (threadIdx.x + kCache * kThreads) * 8; k < K; k += kThreads * 8) {
+        float w[8];
+        load8<ADT>(A, row + k, w);
+        emit(k, w);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
