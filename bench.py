@@ -248,6 +248,8 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
     import torch
 
     import weight_quantized_gemm_gb300 as qg
+    if args.decode_max_m:
+        qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, args.decode_max_m)
     device = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device)
     tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
@@ -384,6 +386,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
+    ap.add_argument("--k", type=int, default=0, help="override the workload's K (e.g. the MNN shape grid)")
+    ap.add_argument("--n", type=int, default=0, help="override the workload's N (e.g. the MNN shape grid)")
+    ap.add_argument("--decode-max-m", type=int, default=0,
+                    help="QGEMM_OPT_DECODE_MAX_M for the run (the decode / tensor-core crossover)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--print-src-hash", action="store_true", help="print the dominant kernel's source hash and exit")
@@ -394,9 +400,9 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
-    if args.m:
+    if args.m or args.k or args.n:
         import dataclasses
-        w = dataclasses.replace(w, M=args.m)
+        w = dataclasses.replace(w, M=args.m or w.M, K=args.k or w.K, N=args.n or w.N)
 
     if args.print_src_hash:
         print(kernel_of(w), src_hash(kernel_of(w)))

@@ -169,6 +169,13 @@ int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, i
  * The setting is process-wide. */
 #define QGEMM_OPT_LAUNCH_OVERLAP 1
 
+/* QGEMM_OPT_DECODE_MAX_M (default 16, range 16..1024). Layers with M up to this value (and
+ * 16-bit activations) run on the weight-streaming decode kernels, in launches of 16 rows of A;
+ * larger M on the tensor-core kernel. A larger value trades extra weight reads (one per 16 rows)
+ * for using every SM when N offers few 128-channel tiles. The setting is process-wide; it
+ * changes qgemm_workspace_bytes for the shapes it moves. */
+#define QGEMM_OPT_DECODE_MAX_M 2
+
 /* Set an option; returns its previous value, or QGEMM_ERR_ARG for an unknown option or value. */
 int qgemm_set_option(int option, int value);
 

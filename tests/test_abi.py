@@ -103,6 +103,13 @@ def test_options():
     assert qg.qgemm_get_option(qg.OPT_LAUNCH_OVERLAP) == 1
     assert qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 0) == 1
     assert qg.load().qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 2) == -1
+    assert qg.qgemm_get_option(qg.OPT_DECODE_MAX_M) == 16
+    ws16 = qg.qgemm_workspace_bytes(32, 4096, 256, qg.MODE_INT4, 64, qg.BF16, qg.BF16)
+    assert qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, 64) == 16     # M = 32 now runs on the decode kernels
+    assert qg.qgemm_workspace_bytes(32, 4096, 256, qg.MODE_INT4, 64, qg.BF16, qg.BF16) != ws16
+    assert qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, 16) == 64
+    assert qg.load().qgemm_set_option(qg.OPT_DECODE_MAX_M, 8) == -1
+    assert qg.load().qgemm_set_option(qg.OPT_DECODE_MAX_M, 2048) == -1
     assert qg.load().qgemm_set_option(99, 0) == -1
     assert qg.load().qgemm_get_option(99) == -1
 

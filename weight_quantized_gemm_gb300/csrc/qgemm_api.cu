@@ -13,6 +13,7 @@ namespace {
 
 thread_local char g_last_error[256] = "";
 std::atomic<int> g_opt_overlap{0};
+std::atomic<int> g_opt_decode_max_m{16};
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -63,7 +64,8 @@ enum Path { PATH_F32, PATH_DECODE, PATH_PREFILL };
 Path choose_path(int M, int K, int N, int mode, int a_dtype) {
     if (a_dtype == QGEMM_F32) return PATH_F32;
     const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
-    if (M > 16 && qg::prefill_supported(M, K, N, fmt, a_dtype)) return PATH_PREFILL;
+    if (M > g_opt_decode_max_m.load(std::memory_order_relaxed) && qg::prefill_supported(M, K, N, fmt, a_dtype))
+        return PATH_PREFILL;
     return PATH_DECODE;
 }
 
@@ -88,11 +90,16 @@ int qgemm_set_option(int option, int value) {
         if (value != 0 && value != 1) return fail(QGEMM_ERR_ARG, "option %d takes 0 or 1, got %d", option, value);
         return g_opt_overlap.exchange(value);
     }
+    if (option == QGEMM_OPT_DECODE_MAX_M) {
+        if (value < 16 || value > 1024) return fail(QGEMM_ERR_ARG, "option %d takes 16..1024, got %d", option, value);
+        return g_opt_decode_max_m.exchange(value);
+    }
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
 int qgemm_get_option(int option) {
     if (option == QGEMM_OPT_LAUNCH_OVERLAP) return g_opt_overlap.load();
+    if (option == QGEMM_OPT_DECODE_MAX_M) return g_opt_decode_max_m.load();
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
