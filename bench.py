@@ -250,6 +250,8 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
     import weight_quantized_gemm_gb300 as qg
     if args.decode_max_m:
         qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, args.decode_max_m)
+    if args.no_split_k:
+        qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
     device = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device)
     tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
@@ -390,6 +392,8 @@ def main():
     ap.add_argument("--n", type=int, default=0, help="override the workload's N (e.g. the MNN shape grid)")
     ap.add_argument("--decode-max-m", type=int, default=0,
                     help="QGEMM_OPT_DECODE_MAX_M for the run (the decode / tensor-core crossover)")
+    ap.add_argument("--no-split-k", action="store_true",
+                    help="QGEMM_OPT_SPLIT_K = 0: the tensor-core kernel never splits K")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--print-src-hash", action="store_true", help="print the dominant kernel's source hash and exit")

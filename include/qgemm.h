@@ -83,9 +83,13 @@ size_t qgemm_packed_bytes(int K, int N, int mode, int w_dtype);
  * of K. */
 size_t qgemm_table_bytes(int K, int N, int mode, int block);
 
-/* Bytes of scratch device memory qgemm_run needs for this call (0 if none). The decode
- * path needs it only when it splits K across thread blocks (small N); W4A8 needs it for the
- * quantized activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums). */
+/* Bytes of scratch device memory qgemm_run uses for this call (0 if none). The decode path
+ * needs it when it splits K across thread blocks (small N); W4A8 needs it for the quantized
+ * activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums). The tensor-core
+ * path (M above QGEMM_OPT_DECODE_MAX_M) uses it for float32 partial sums when it splits K
+ * (mid-sized M, few 128-channel tiles): splits*M*N*4 bytes. That part is optional: qgemm_run
+ * given less scratch splits K fewer times (down to none), which changes only the float32
+ * summation order of the result. */
 size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype);
 
 /* ---------------------------------------------------------------- weight preparation */
@@ -147,8 +151,10 @@ size_t qgemm_w4a8_acc_workspace_bytes(int M, int K);
  * a fixed array inside the library (QGEMM_NOALLOC_SCRATCH_BYTES, 256-byte aligned) that every
  * GPU which loads the library keeps until the process exits. No call allocates or frees device
  * memory.
- *   - A call whose scratch need (qgemm_workspace_bytes) exceeds the array is rejected with
- *     QGEMM_ERR_WORKSPACE before anything is enqueued. Calls that need no scratch always fit.
+ *   - A call whose required scratch exceeds the array is rejected with QGEMM_ERR_WORKSPACE
+ *     before anything is enqueued; calls that need no scratch always fit. The required part is
+ *     qgemm_workspace_bytes less the tensor-core path's optional split-K partial sums, which
+ *     are cut to what the array holds.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *     with that device current; make that first call before capturing a stream into a graph.
  *   - All calls share the one array and leave their data in it. Every byte a call reads from it
@@ -175,6 +181,13 @@ int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, i
  * for using every SM when N offers few 128-channel tiles. The setting is process-wide; it
  * changes qgemm_workspace_bytes for the shapes it moves. */
 #define QGEMM_OPT_DECODE_MAX_M 2
+
+/* QGEMM_OPT_SPLIT_K (default 1). When 1, the tensor-core kernel splits K across thread blocks
+ * for shapes whose output tiles (128 channels x up to 256 rows) fill less than one wave of the
+ * GPU's SMs; each split writes float32 partial sums to the workspace and a second kernel adds
+ * them in a fixed order and rounds once. When 0, it never splits (no workspace needed). The
+ * setting is process-wide; it changes qgemm_workspace_bytes for the shapes it affects. */
+#define QGEMM_OPT_SPLIT_K 3
 
 /* Set an option; returns its previous value, or QGEMM_ERR_ARG for an unknown option or value. */
 int qgemm_set_option(int option, int value);

@@ -110,6 +110,16 @@ def test_options():
     assert qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, 16) == 64
     assert qg.load().qgemm_set_option(qg.OPT_DECODE_MAX_M, 8) == -1
     assert qg.load().qgemm_set_option(qg.OPT_DECODE_MAX_M, 2048) == -1
+    # the tensor-core path's split-K partials: M = 64, N = 4096 gives 32 tiles of 128 channels x
+    # 64 rows, so K = 2560 (40 stages of 64) is split 4 ways to fill one wave of 152 SMs
+    assert qg.qgemm_get_option(qg.OPT_SPLIT_K) == 1
+    assert qg.qgemm_workspace_bytes(64, 2560, 4096, qg.MODE_INT4, 64, qg.F16, qg.F16) == 4 * 64 * 4096 * 4
+    assert qg.qgemm_workspace_bytes(64, 256, 4096, qg.MODE_INT4, 64, qg.F16, qg.F16) == 0       # 4 stages: no split
+    assert qg.qgemm_workspace_bytes(1024, 4096, 4096, qg.MODE_INT4, 64, qg.F16, qg.F16) == 0    # 128 tiles already
+    assert qg.qgemm_set_option(qg.OPT_SPLIT_K, 0) == 1
+    assert qg.qgemm_workspace_bytes(64, 2560, 4096, qg.MODE_INT4, 64, qg.F16, qg.F16) == 0
+    assert qg.qgemm_set_option(qg.OPT_SPLIT_K, 1) == 0
+    assert qg.load().qgemm_set_option(qg.OPT_SPLIT_K, 2) == -1
     assert qg.load().qgemm_set_option(99, 0) == -1
     assert qg.load().qgemm_get_option(99) == -1
 

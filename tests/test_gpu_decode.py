@@ -34,12 +34,13 @@ def gpu_pack(W: np.ndarray, mode: int, block: int, w_dtype: int = 0):
     return Bp, T
 
 
-def gpu_run(M, K, N, mode, block, A_np, a_dtype, Bp, T, c_dtype):
+def gpu_run(M, K, N, mode, block, A_np, a_dtype, Bp, T, c_dtype, ws_bytes=None):
+    """qgemm_run with the workspace qgemm_workspace_bytes asks for, or with ws_bytes of it."""
     A = torch_from(A_np, a_dtype)
     # NaN-poisoned output followed by a guard band: every output must be written, nothing after it
     flat = torch.full((M * N + CANARY,), float("nan"), dtype=torch_dtype(c_dtype), device=DEV)
     C = flat[: M * N].view(M, N)
-    wsb = qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, c_dtype)
+    wsb = qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, c_dtype) if ws_bytes is None else ws_bytes
     ws = torch.empty(wsb + 4096, dtype=torch.uint8, device=DEV).fill_(0xA5) if wsb else None
     qg.qgemm_run(M, K, N, mode, block, A, a_dtype, Bp, T, C, c_dtype, ws, wsb)
     assert qg.qgemm_status() == 0

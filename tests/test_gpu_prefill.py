@@ -35,6 +35,41 @@ def test_prefill_output_dtypes(c_dtype):
     layer_case(130, 512, 200, 1, 64, synth.F16, c_dtype)
 
 
+# ---------------------------------------------------------------- split-K (mid-sized M)
+# Shapes with fewer 128-channel x BN-row tiles than SMs split K across blocks: each split adds its
+# stages into float32 partial sums, a second kernel adds the splits in order and rounds once.
+@pytest.mark.parametrize("M,K,N,mode,block,a_dtype,splits", [
+    (40, 1088, 130, 1, 64, synth.F16, 2),      # splits of 8 and 9 stages; rows not 16-byte multiples
+    (64, 2560, 4096, 1, 64, synth.F16, 4),     # partials stored by TMA
+    (96, 1600, 1000, 2, 0, synth.BF16, 3),     # uneven splits (8, 8, 9), per-channel int8
+    (48, 2048, 384, 1, 128, synth.BF16, 4),    # bf16 hi/lo weight parts, K-blocks across splits
+    (33, 1024, 256, 0, 0, synth.BF16, 2),      # float mode
+])
+def test_prefill_split_k(M, K, N, mode, block, a_dtype, splits):
+    assert qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, a_dtype) == splits * M * N * 4
+    layer_case(M, K, N, mode, block, a_dtype, a_dtype)
+
+
+def test_prefill_split_k_less_workspace():
+    """Less scratch than asked for: fewer splits (3 of 5, then none), each result within the bar."""
+    M, K, N, mode, block = 64, 2560, 512, 1, 64
+    w = synth.Workload("t", M, K, N, mode, block, synth.F16, synth.F16, 3, 4)
+    A_np, W_np = synth.make_activations(w), synth.make_weights(w)
+    ref = oracle.reference_layer(mode, block, A_np, synth.F16, W_np, 0)
+    Bp, T = gpu_pack(W_np, mode, block)
+    full = qg.qgemm_workspace_bytes(M, K, N, mode, block, synth.F16, synth.F16)
+    assert full == 5 * M * N * 4
+    for wsb in (full, 3 * M * N * 4 + 100, M * N * 4 + 4, 0):
+        got = gpu_run(M, K, N, mode, block, A_np, synth.F16, Bp, T, synth.F16, ws_bytes=wsb)
+        check_close(got, ref["R"], synth.F16, synth.F16, f"workspace {wsb}")
+    prev = qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
+    try:
+        got = gpu_run(M, K, N, mode, block, A_np, synth.F16, Bp, T, synth.F16)
+        check_close(got, ref["R"], synth.F16, synth.F16, "split-K off")
+    finally:
+        qg.qgemm_set_option(qg.OPT_SPLIT_K, prev)
+
+
 def _sampled_case(w: synth.Workload, npts: int = 4096, seed: int = 0):
     """Full-size layer on the GPU, checked at sampled (m, n) points against the oracle."""
     A_np = synth.make_activations(w)

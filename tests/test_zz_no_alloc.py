@@ -57,6 +57,22 @@ def test_noalloc_matches_run_twice(w):
         check_close(to_numpy_values(out, w.c_dtype), R, w.a_dtype, w.c_dtype, f"noalloc {w.name}")
 
 
+def test_noalloc_cuts_tensor_core_splits():
+    """The tensor-core path's split-K partials are optional scratch: M = 128, N = 4096, K = 4096
+    prefers 4 splits (8 MiB of partials), the built-in array holds 2; the call runs with 2."""
+    import oracle
+    w = synth.Workload("prefill_splitk", 128, 4096, 4096, synth.MODE_INT4, 64, synth.BF16, synth.BF16, 7, 8)
+    need = qg.qgemm_workspace_bytes(w.M, w.K, w.N, w.mode, w.block, w.a_dtype, w.c_dtype)
+    assert need == 4 * w.M * w.N * 4 > qg.NOALLOC_SCRATCH_BYTES
+    A_np, W_np = synth.make_activations(w), synth.make_weights(w)
+    ref = oracle.reference_layer(w.mode, w.block, A_np, w.a_dtype, W_np, 0)
+    A, Bp, T = _prepare(w)
+    out = torch.full((w.M, w.N), float("nan"), dtype=torch_dtype(w.c_dtype), device=DEV)
+    qg.qgemm_run_noalloc(w.M, w.K, w.N, w.mode, w.block, A, w.a_dtype, Bp, T, out, w.c_dtype)
+    assert qg.qgemm_status() == 0
+    check_close(to_numpy_values(out, w.c_dtype), ref["R"], w.a_dtype, w.c_dtype, "noalloc split-K")
+
+
 def test_noalloc_refuses_oversized_call():
     # W4A8 at M = 2048, K = 4096 needs ~16.8 MB of scratch, more than the built-in array
     w = synth.Workload("w4a8_big", 2048, 4096, 128, synth.MODE_W4A8, 0, synth.BF16, synth.BF16, 0, 1)

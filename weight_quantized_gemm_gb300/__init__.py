@@ -15,13 +15,14 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
 MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
 OPT_LAUNCH_OVERLAP = 1
 OPT_DECODE_MAX_M = 2
+OPT_SPLIT_K = 3
 NOALLOC_SCRATCH_BYTES = 4 << 20
 F32, F16, BF16 = 0, 1, 2
 OK = 0

@@ -146,19 +146,23 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
             if (e != cudaSuccess) return e;
             continue;
         }
-        const size_t count = (size_t)c.M * c.N;
-        const int threads = 256;
-        const size_t want = (count + threads - 1) / threads;
-        const int blocks = (int)(want < 4096 ? want : 4096);
-        switch (c.c_dtype) {
-            case DT_F32: splitk_reduce_kernel<DT_F32><<<blocks, threads, 0, s>>>(c.partial, c.splits, count, c.C); break;
-            case DT_F16: splitk_reduce_kernel<DT_F16><<<blocks, threads, 0, s>>>(c.partial, c.splits, count, c.C); break;
-            default: splitk_reduce_kernel<DT_BF16><<<blocks, threads, 0, s>>>(c.partial, c.splits, count, c.C); break;
-        }
-        e = cudaGetLastError();
+        e = launch_splitk_reduce(c.partial, c.splits, (size_t)c.M * c.N, c.C, c.c_dtype, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, void* C, int c_dtype,
+                                 cudaStream_t s) {
+    const int threads = 256;
+    const size_t want = (count + threads - 1) / threads;
+    const int blocks = (int)(want < 4096 ? want : 4096);
+    switch (c_dtype) {
+        case DT_F32: splitk_reduce_kernel<DT_F32><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
+        case DT_F16: splitk_reduce_kernel<DT_F16><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
+        default: splitk_reduce_kernel<DT_BF16><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s) {

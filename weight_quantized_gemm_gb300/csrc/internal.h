@@ -51,6 +51,10 @@ struct DecodeArgs {
 // table's K-group (K for per-channel).
 int decode_splits(int M, int K, int N, int fmt, int block);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// C[i] = sum over y = 0 .. splits-1, in that order, of partial[y * count + i] (float32), rounded
+// once to c_dtype.
+cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, void* C, int c_dtype,
+                                 cudaStream_t s);
 // Exact float32 CUDA-core kernel (any activation dtype, any M); used for f32 activations.
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
 
@@ -61,7 +65,11 @@ struct PrefillArgs {
     const void* Bp;
     const float* T;
     void* C;
+    float* partial;   // [splits][M][N] f32 partial sums when splits > 1
+    int splits;       // K-splits across thread blocks (>= 1), from prefill_splits
 };
+// K-splits the tensor-core kernel uses for this shape (1 = none); host-only, no GPU needed.
+int prefill_splits(int M, int K, int N, int fmt);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 bool prefill_supported(int M, int K, int N, int fmt, int a_dtype);
 

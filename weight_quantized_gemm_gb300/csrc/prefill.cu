@@ -4,15 +4,18 @@
 // «为什么用 Conv1x1 来测 GEMM») is computed transposed, D[n][m] = sum_k W[n][k] * A[m][k], so that
 // the operand that needs work before it can be multiplied -- the packed weight -- is the MMA's
 // A operand and lives in tensor memory, while the activations stream in by TMA:
-//   - dequant warps read the packed weight rows of a 128-channel tile straight from global
-//     memory, rebuild w = q * scale + offset in float32 (one rounding to the activation's 16-bit
-//     type) and write them into a TMEM stage with tcgen05.st (no shared-memory traffic);
-//   - a TMA warp loads the matching 64-wide K slice of A (up to 256 rows, 128-byte swizzle)
-//     into a shared-memory stage;
+//   - a TMA warp loads, per pipeline stage, the stage's K slice of A (up to 256 rows, 128-byte
+//     swizzle), the packed weight rows of the 128-channel tile and their {offset, scale} table
+//     entries into shared memory; a stage is one or two 64-wide sub-stages of K;
+//   - dequant warps rebuild w = q * scale + offset in float32 (one rounding to the activation's
+//     16-bit type) and write them into a TMEM stage with tcgen05.st;
 //   - one thread issues tcgen05.mma (kind::f16, M = 128, N = tile rows of A, K = 16 per
 //     instruction) with A from TMEM and B from shared memory, accumulating in TMEM, and
 //     commits each stage back to the producers;
-//   - after the last stage the dequant warps read the accumulator with tcgen05.ld and store C.
+//   - after the last stage the dequant warps read the accumulator with tcgen05.ld, stage the
+//     tile in shared memory and store it (one TMA store where the rows allow).
+// Shapes whose tiles fill less than one wave of SMs split K across blocks (grid z): each split
+// writes float32 partial sums and a second kernel adds them in a fixed order.
 // W4A8 ("W4 解包为 INT8 ... S8×S8→S32", «测试用例与注册机制») uses the same kernel with the 4-bit
 // codes as exact f16 integers and the activation codes as exact f16 integers: every product is
 // an integer below 2^11 and every partial sum an integer below 2^24, so the float32 tensor-core
@@ -40,13 +43,11 @@ namespace pf {
 constexpr int kBM = 128;              // output channels per tile (MMA M)
 constexpr int kBK = 64;               // K per pipeline stage
 constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
-constexpr int kStageBytesX = kMaxBN * kBK * 2;
 constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpiThreads = (kWarps - 2) * 32;   // dequant + epilogue threads
 constexpr int kTmemCols = 512;
-constexpr int kAccCol = 0;            // accumulator columns [0, BN)
-constexpr int kACol = 256;            // A stages from column 256: 32 columns each (64 with a low part)
+constexpr int kAccCol = 0;            // accumulator columns [0, BN); the A stages follow
 
 enum Wf { WF_INT4 = 0, WF_INT8 = 1, WF_FLOAT = 2, WF_CODES4 = 3 };
 enum Epi { EPI_STORE = 0, EPI_W4A8 = 1, EPI_ACC = 2 };
@@ -60,6 +61,8 @@ struct Params {
     const int32_t* rowsum;    // W4A8: per-row sum of activation codes
     int32_t* acc;             // EPI_ACC output
     int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
+    int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
+    int tblocks;              // K-blocks per table box (min(SUB, nb))
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -272,73 +275,100 @@ __device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
         static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
 }
 
-// Shared-memory stage: the A (activation) box [BN rows][128 B] at offset 0 and the packed
-// weight box at kWOff: [128 rows][stage bytes of one row] for the quantized formats, or the
-// 16-bit weights [128 rows][128 B] with the 128-byte swizzle in float mode (then read by the
-// MMA directly as its A operand).
-constexpr int kWOff = kStageBytesX;
-constexpr size_t kSmemMax = 232448;   // opt-in shared memory per block
+// Shared-memory stage of SUB sub-stages (SUB x 64 of K), at a multiple of 1024 bytes:
+//   [SUB activation boxes, each [BN rows][128 B] with the 128-byte swizzle]
+//   [weights: one box [128 rows][SUB x row bytes of a sub-stage] for the quantized formats, or
+//    (float mode, SUB = 1) the 16-bit weights [128 rows][128 B] with the 128-byte swizzle, read by
+//    the MMA directly as its A operand]
+//   [formats with a table: the {offset, scale} entries of the stage's (up to) SUB K-blocks for the
+//    tile's 128 channels, [8 groups of 16][SUB x 32 floats] in the grouped table layout]
+// One stage is one round of the pipeline's barriers, so SUB = 2 halves the waits, arrivals and
+// commits per unit of K; the ring holds as many stages as shared and tensor memory allow.
+constexpr size_t kSmemMax = 232448;                 // opt-in shared memory per block
+constexpr int kTail = 256 + kMaxBN * 8;              // barriers + W4A8 row factors after the ring
+constexpr int kRing = (int)kSmemMax - kTail;         // bytes for the stages
+constexpr int kMaxStages = 8;
 template <int WF>
-struct WBox {
+struct WBox {   // bytes of one channel row of one 64-wide sub-stage
     static constexpr int kRowBytes = (WF == WF_INT4 || WF == WF_CODES4) ? kBK / 2 : (WF == WF_INT8 ? kBK : 2 * kBK);
 };
-// Ring depth per format: a stage is the activation box plus only the weight bytes the format
-// needs (4 KB for 4-bit codes, 8 KB for 8-bit, 16 KB for 16-bit weights), as many stages as
-// shared memory holds (6, 5, 4), and no more than the TMEM columns left for A stages beside the
-// accumulator allow (8 stages of 32 columns, 4 of 64 with the bf16 hi/lo split). The deeper ring
-// covers the TMA latency plus the dequantization of a stage, which only starts once its weights
-// have landed.
+template <int WF, bool BF, int SUB>
+struct Geo {
+    static constexpr bool kTable = WF == WF_INT4 || WF == WF_INT8;
+    static constexpr int kWBytes = kBM * SUB * WBox<WF>::kRowBytes;
+    static constexpr int kTBytes = kTable ? SUB * (kBM / 16) * 128 : 0;
+    static constexpr int kCols = SUB * Split<WF, BF>::kStageCols;   // TMEM columns of one A stage
+    static constexpr int stage_bytes(int BN) { return SUB * BN * kBK * 2 + kWBytes + kTBytes; }
+    // stages in the ring for tile height BN: what shared memory holds, and what tensor memory
+    // holds beside the BN accumulator columns
+    static constexpr int stages(int BN) {
+        return kRing / stage_bytes(BN) < (kTmemCols - BN) / kCols
+                   ? (kRing / stage_bytes(BN) < kMaxStages ? kRing / stage_bytes(BN) : kMaxStages)
+                   : ((kTmemCols - BN) / kCols < kMaxStages ? (kTmemCols - BN) / kCols : kMaxStages);
+    }
+};
+// The kernel's shape for tile height BN, fixed at compile time: two 64-wide sub-stages per stage
+// (half the barrier rounds per unit of K) where the ring still holds at least kMinSub2Stages of
+// them -- small tiles, whose stages are short and whose per-round costs dominate; large tiles keep
+// 64-wide stages, whose finer-grained ring refills sooner.
+constexpr int kMinSub2Stages = 5;
+template <int WF, bool BF, int BN>
+struct Plan {
+    static constexpr int kSub = (WF != WF_FLOAT && Geo<WF, BF, 2>::stages(BN) >= kMinSub2Stages) ? 2 : 1;
+    using G = Geo<WF, BF, kSub>;
+    static constexpr int kStages = G::stages(BN);
+    static constexpr int kStageBytes = G::stage_bytes(BN);
+    static_assert(WF != WF_FLOAT || kSub == 1, "float mode loads one swizzled weight box per stage");
+    static_assert(kStages >= 2 && kStages <= kMaxStages, "ring of at least two stages");
+    static_assert(kStages * kStageBytes <= kRing, "ring fits in shared memory");
+    static_assert(BN + kStages * G::kCols <= kTmemCols, "accumulator and A stages fit in TMEM");
+    static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle atoms)");
+};
 struct Maps {                 // the kernel's tensor maps
     CUtensorMap a;            // activations
     CUtensorMap w;            // packed weights
     CUtensorMap t;            // grouped {offset, scale} table (formats with a table)
     CUtensorMap c;            // the output, when Params::c_tma (stored by TMA from the staged tile)
 };
-// The {offset, scale} entries of a stage's K-block for the tile's 128 channels (8 groups of 16,
-// 128 bytes each in the grouped table layout) follow the weight box: one more TMA box.
-template <int WF>
-struct TBox {
-    static constexpr bool kOn = WF == WF_INT4 || WF == WF_INT8;
-    static constexpr int kOff = kWOff + kBM * WBox<WF>::kRowBytes;
-    static constexpr int kBytes = kOn ? kBM * 8 : 0;
-};
-template <int WF, bool BF>
-struct Ring {
-    static constexpr int kStageBytes = kStageBytesX + kBM * WBox<WF>::kRowBytes + TBox<WF>::kBytes;   // multiples of 1024
-    static constexpr int kSmemStages = (int)((kSmemMax - 256 - kMaxBN * 8) / kStageBytes);
-    static constexpr int kTmemStages = (kTmemCols - kACol) / Split<WF, BF>::kStageCols;
-    static constexpr int kStages = kSmemStages < kTmemStages ? kSmemStages : kTmemStages;
-    static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + kMaxBN * 8;   // + W4A8 row factors
-};
 
-// One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), all of K.
-template <int WF, bool BF, int EPI, int CDT>
+// One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), and the
+// stages of K-split z (all of K when p.splits == 1).
+template <int WF, bool BF, int EPI, int CDT, int BN>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Maps maps, Params p) {
+    using P = Plan<WF, BF, BN>;
+    using G = typename P::G;
+    constexpr int SUB = P::kSub, S = P::kStages;
+    constexpr uint32_t SB = P::kStageBytes;
     constexpr bool kDequant = WF != WF_FLOAT;          // weights go through the dequant warps into TMEM
-    constexpr bool kTable = WF == WF_INT4 || WF == WF_INT8;
-    constexpr int kCols = Split<WF, BF>::kStageCols;
-    constexpr int kStages = Ring<WF, BF>::kStages, kStageBytes = Ring<WF, BF>::kStageBytes;
+    constexpr int kRowB = WBox<WF>::kRowBytes;
+    constexpr int kLo = SUB * 32;                      // TMEM column of the low parts in an A stage (Split)
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BN = p.BN;
+    constexpr uint32_t kABytes = (uint32_t)BN * kBK * 2;   // one activation box
+    constexpr uint32_t w_off = SUB * kABytes, t_off = w_off + G::kWBytes;
     const int n_tile = blockIdx.x * kBM, m_tile = blockIdx.y * BN;
-    const int nk = p.K / kBK;
+    const int nsub = p.K / kBK;                        // 64-wide sub-stages of K
+    const int nst = (nsub + SUB - 1) / SUB;            // stages (the last may be half past K: reads 0)
+    // split z covers stages [ks0, ks0 + nks); the ring counts stages from 0 within the split
+    const int ks0 = (int)((long long)nst * blockIdx.z / p.splits);
+    const int nks = (int)((long long)nst * (blockIdx.z + 1) / p.splits) - ks0;
+    const int bpb = p.block / kBK;                     // sub-stages per table block
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    // bars: full[kStages] (both boxes landed) | full_a[kStages] (TMEM A stage written) |
-    //       empty[kStages] (MMAs of the stage done) | acc_full
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
+    // bars: full[S] (the stage's boxes landed) | full_a[S] (TMEM A stage written) |
+    //       empty[S] (MMAs of the stage done) | acc_full
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
-    float2* rowf = reinterpret_cast<float2*>(smem + kStages * kStageBytes + 256);
+    float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
     const uint32_t st_s = smem_u32(smem);
     auto full_x = [&](int s) { return smem_u32(bars + s); };
-    auto full_a = [&](int s) { return smem_u32(bars + kStages + s); };
-    auto empty = [&](int s) { return smem_u32(bars + 2 * kStages + s); };
-    const uint32_t acc_full = smem_u32(bars + 3 * kStages);
+    auto full_a = [&](int s) { return smem_u32(bars + kMaxStages + s); };
+    auto empty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + s); };
+    const uint32_t acc_full = smem_u32(bars + 3 * kMaxStages);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full_x(s), 1);
             mbar_init(full_a(s), 8);   // one arrival per dequant warp
             mbar_init(empty(s), 1);    // one tcgen05.commit per use
@@ -348,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
         ptx::prefetch_tmap(&maps.w);
-        if constexpr (TBox<WF>::kOn) ptx::prefetch_tmap(&maps.t);
+        if constexpr (G::kTable) ptx::prefetch_tmap(&maps.t);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -358,38 +388,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t a_col = tmem + (uint32_t)BN;        // A stages follow the BN accumulator columns
 
     if (warp == 0) {
-        // ---------------- TMA producer: the A slice, the weight slice and (formats with a table)
-        // the stage's {offset, scale} entries of each stage
+        // ---------------- TMA producer: per stage the SUB activation boxes, the weight box and
+        // (formats with a table) the {offset, scale} entries of the stage's K-blocks
         if (lane == 0) {
-            const uint32_t bytes =
-                (uint32_t)BN * kBK * 2 + (uint32_t)kBM * WBox<WF>::kRowBytes + (uint32_t)TBox<WF>::kBytes;
-            const int spb = p.block / kBK;   // stages per table block (the block is a multiple of 64)
-            int issued = 0, tb = 0, tc = 0;  // table block of stage ks, and ks's position in it
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+            const uint32_t bytes = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
+            int issued = 0, s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nks; ++i) {
+                const int ks = ks0 + i;
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+                const uint32_t st = st_s + (uint32_t)s * SB;
                 mbar_expect_tx(full_x(s), bytes);
-                tma_load_2d(st_s + s * kStageBytes, &maps.a, ks * kBK, m_tile, full_x(s));
+#pragma unroll
+                for (int j = 0; j < SUB; ++j)
+                    tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
                 // weight box: x in bytes for the packed formats, in elements for float mode
-                tma_load_2d(st_s + s * kStageBytes + kWOff, &maps.w,
-                            WF == WF_FLOAT ? ks * kBK : ks * WBox<WF>::kRowBytes, n_tile, full_x(s));
-                if constexpr (TBox<WF>::kOn) {
-                    // 8 groups of 16 channels, block tb: x = 32 floats per block, y = group
-                    tma_load_2d(st_s + s * kStageBytes + TBox<WF>::kOff, &maps.t, 32 * tb, n_tile / 16, full_x(s));
-                    if (++tc == spb) {
-                        tc = 0;
-                        ++tb;
-                    }
-                }
-                issued = ks + 1;
+                tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
+                if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
+                                           // (the box holds tblocks K-blocks, the stage's first one first)
+                    tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
+                issued = i + 1;
+                if (++s == S) { s = 0; ph ^= 1u; }
             }
             if (*abort_flag) {   // let the copies already issued land before the block exits
-                for (int ks = issued - kStages < 0 ? 0 : issued - kStages; ks < issued; ++ks) {
+                for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
                     volatile int never = 0;
-                    mbar_wait(full_x(ks % kStages), (uint32_t)(ks / kStages) & 1u, &never);
+                    mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never);
                 }
             }
         }
@@ -397,29 +424,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(BF, BN, kBM);
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nks; ++i) {
                 if constexpr (kDequant)
                     if (!mbar_wait(full_a(s), ph, abort_flag)) break;
                 if (!mbar_wait(full_x(s), ph, abort_flag)) break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_desc(st_s + s * kStageBytes);
+                const uint32_t st = st_s + (uint32_t)s * SB;
+                const uint32_t as = a_col + (uint32_t)(s * G::kCols);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    if constexpr (kDequant) {
-                        mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + kk * 8, bdesc + (uint64_t)(2 * kk), idesc,
-                               (ks | kk) != 0);
-                        if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
-                            mma_ts(tmem + kAccCol, tmem + kACol + s * kCols + 32 + kk * 8, bdesc + (uint64_t)(2 * kk),
-                                   idesc, 1u);
-                    } else {
-                        const uint64_t adesc = sw128_desc(st_s + s * kStageBytes + kWOff);
-                        mma_ss(tmem + kAccCol, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                               (ks | kk) != 0);
+                for (int j = 0; j < SUB; ++j) {
+                    const uint64_t bdesc = sw128_desc(st + j * kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t acc = (i | j | kk) != 0;
+                        if constexpr (kDequant) {
+                            mma_ts(tmem, as + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, acc);
+                            if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
+                                mma_ts(tmem, as + kLo + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, 1u);
+                        } else {
+                            const uint64_t adesc = sw128_desc(st + w_off);
+                            mma_ss(tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc, acc);
+                        }
                     }
                 }
                 mma_commit(empty(s));
+                if (++s == S) { s = 0; ph ^= 1u; }
             }
             mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
         }
@@ -433,34 +464,54 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
         }
-        // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each stage
+        // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each
+        // 64-wide sub-stage
         const int q = warp & 3, h = (warp - 2) >> 2;
         const int r = 32 * q + lane;                 // row inside the tile
         const int row = n_tile + r;
         const int rc = row < p.N ? row : p.N - 1;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         if constexpr (kDequant) {
-            for (int ks = 0; ks < nk; ++ks) {
-                const int s = ks % kStages;
-                const uint32_t ph = (uint32_t)(ks / kStages) & 1u;
+            int s = 0;
+            uint32_t ph = 0;
+            int pos = (ks0 * SUB) % bpb;             // first sub-stage of the stage, within its K-block
+            for (int i = 0; i < nks; ++i) {
                 if (!mbar_wait(full_x(s), ph, abort_flag)) break;
-                const uint32_t wsrc = st_s + s * kStageBytes + kWOff + r * WBox<WF>::kRowBytes +
-                                      h * (WBox<WF>::kRowBytes / 2);
-                uint4 raw[4];
-                raw[0] = lds128u(wsrc);
-                if constexpr (WF == WF_INT8) raw[1] = lds128u(wsrc + 16);
-                float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and stage
-                if constexpr (TBox<WF>::kOn) e = lds64f(st_s + s * kStageBytes + TBox<WF>::kOff + r * 8);
-                uint32_t out[16], rest[16];
-                convert32<WF, BF>(raw, e.y, e.x, out, rest);
+                const uint32_t st = st_s + (uint32_t)s * SB;
+                uint32_t out[SUB][16], rest[SUB][16];
+#pragma unroll
+                for (int j = 0; j < SUB; ++j) {
+                    uint4 raw[4];
+                    const uint32_t wsrc = st + w_off + r * (SUB * kRowB) + j * kRowB + h * (kRowB / 2);
+                    raw[0] = lds128u(wsrc);
+                    if constexpr (WF == WF_INT8) raw[1] = lds128u(wsrc + 16);
+                    float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and sub-stage
+                    if constexpr (G::kTable) {
+                        // K-block of the sub-stage in the box (the box starts at the stage's
+                        // first block); a sub-stage past K (its weights and activations read 0)
+                        // keeps the last block of the box
+                        const int d = (j == 0 || pos + j < bpb) ? 0 : min(1, p.tblocks - 1);
+                        e = lds64f(st + t_off + (r >> 4) * (p.tblocks * 128) + d * 128 + (r & 15) * 8);
+                    }
+                    convert32<WF, BF>(raw, e.y, e.x, out[j], rest[j]);
+                }
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                tmem_st16(tmem + lane_base + kACol + s * kCols + 16 * h, out);
-                if constexpr (Split<WF, BF>::kOn) tmem_st16(tmem + lane_base + kACol + s * kCols + 32 + 16 * h, rest);
+                const uint32_t dst = a_col + lane_base + (uint32_t)(s * G::kCols) + 16 * h;
+#pragma unroll
+                for (int j = 0; j < SUB; ++j) {
+                    tmem_st16(dst + 32 * j, out[j]);
+                    if constexpr (Split<WF, BF>::kOn) tmem_st16(dst + kLo + 32 * j, rest[j]);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a(s));
+                if (++s == S) { s = 0; ph ^= 1u; }
+                if (SUB > 1 || bpb > 1) {
+                    pos += SUB;
+                    while (pos >= bpb) pos -= bpb;
+                }
             }
         }
         // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
@@ -505,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             ptx::fence_proxy_async_smem();
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
             if (ok && threadIdx.x == 64) {
-                ptx::tma_store_2d(&maps.c, n_tile, m_tile, smem_u32(tile));
+                ptx::tma_store_3d(&maps.c, n_tile, m_tile, blockIdx.z, smem_u32(tile));
                 ptx::bulk_commit();
                 ptx::bulk_wait_read();
             }
@@ -515,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
             constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
             constexpr int kChunks = kBM / kPer;               // chunks per tile row
-            uint8_t* out = EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C);
+            uint8_t* out = (EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C)) +
+                           (size_t)blockIdx.z * p.M * p.N * kEsz;
             const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
             for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
                 const int ml = idx / kChunks, c = idx - ml * kChunks;
@@ -563,15 +615,16 @@ cudaError_t make_tmap(CUtensorMap* map, const void* A, bool bf16, int M, int K, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Rows of A per tile (the MMA's N): 64, 128 or 256.
 int pick_bn(int M) {
-    if (M >= 256) return 256;
-    return (M + 63) / 64 * 64;
+    return M <= 64 ? 64 : (M <= 128 ? 128 : 256);
 }
 
 
 // The packed weight rows [N][row bytes] as a 2-D byte (quantized formats) or 16-bit (float mode,
-// 128-byte swizzle) tensor; box = one stage of 128 rows; rows past N read 0.
-cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N, int K) {
+// 128-byte swizzle) tensor; box = one stage (sub sub-stages of 64) of 128 rows; rows past N and
+// bytes past K read 0.
+cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N, int K, int sub) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUresult r;
@@ -585,7 +638,7 @@ cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         const int row_bytes = (wf == WF_INT8) ? K : K / 2;
-        const int box_bytes = (wf == WF_INT8) ? kBK : kBK / 2;
+        const int box_bytes = sub * ((wf == WF_INT8) ? kBK : kBK / 2);
         const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
         const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
         const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kBM};
@@ -598,14 +651,14 @@ cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N
 }
 
 // The grouped {offset, scale} table [ceil(N/16)][nb][16][2] as a 2-D float tensor: x = 32 floats
-// per K-block of a group (16 channels x 2), y = group (stride nb * 128 bytes); box = one K-block
-// of 8 groups (the tile's 128 channels); groups past the end read 0.
-cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb) {
+// per K-block of a group (16 channels x 2), y = group (stride nb * 128 bytes); box = tblocks
+// consecutive K-blocks of 8 groups (the tile's 128 channels); entries past the end read 0.
+cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb, int tblocks) {
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)32 * nb, (cuuint64_t)((N + 15) / 16)};
     const cuuint64_t strides[1] = {(cuuint64_t)nb * 128};
-    const cuuint32_t box[2] = {32, (cuuint32_t)(kBM / 16)};
+    const cuuint32_t box[2] = {(cuuint32_t)(32 * tblocks), (cuuint32_t)(kBM / 16)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(T), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -613,10 +666,11 @@ cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb) {
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// The output [M][N] (bf16 / f16 / f32, or int32 accumulators) as a 2-D tensor; box = one tile of
-// 128 channels x BN rows, matching the staged [rows][128] tile. Only when a row is a whole number
-// of 16-byte units (TMA strides) and the base is 16-byte aligned; else returns false.
-bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN) {
+// The output [depth][M][N] (bf16 / f16 / f32, or int32 accumulators; depth = the K-splits' partial
+// sums, else 1) as a 3-D tensor; box = one tile of 128 channels x BN rows of one slice, matching the
+// staged [rows][128] tile. Only when a row is a whole number of 16-byte units (TMA strides) and
+// the base is 16-byte aligned; else returns false.
+bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN, int depth) {
     const size_t esz = kind == DT_F32 || kind < 0 ? 4 : 2;
     if (((size_t)N * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return false;
     EncodeTiledFn enc = tensor_map_encoder();
@@ -624,31 +678,49 @@ bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN) {
     const CUtensorMapDataType dt = kind < 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32
                                    : (kind == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : (kind == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16));
-    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)N * esz};
-    const cuuint32_t box[2] = {(cuuint32_t)kBM, (cuuint32_t)BN};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, dt, 2, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)depth};
+    const cuuint64_t strides[2] = {(cuuint64_t)N * esz, (cuuint64_t)M * N * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)kBM, (cuuint32_t)BN, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WF, bool BF, int EPI, int CDT>
+template <int WF, bool BF, int EPI, int CDT, int BN>
 cudaError_t launch_k(const Maps& maps, const Params& p, cudaStream_t s) {
-    auto kern = prefill_kernel<WF, BF, EPI, CDT>;
-    constexpr size_t smem = Ring<WF, BF>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = prefill_kernel<WF, BF, EPI, CDT, BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN);
-    kern<<<grid, kThreads, smem, s>>>(maps, p);
+    dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN, p.splits);
+    kern<<<grid, kThreads, kSmemMax, s>>>(maps, p);
     return cudaGetLastError();
 }
 
-template <int WF, bool BF, int EPI>
-cudaError_t launch_cdt(const Maps& maps, const Params& p, int c_dtype, cudaStream_t s) {
+// The weight and table maps for the plan's sub-stages per stage, then the launch for the output
+// type c_dtype (EPI_ACC: int32).
+template <int WF, bool BF, int EPI, int BN>
+cudaError_t launch_bn(Maps maps, Params p, int c_dtype, cudaStream_t s) {
+    using P = Plan<WF, BF, BN>;
+    cudaError_t e = make_wmap(&maps.w, p.Bp, WF, BF, p.N, p.K, P::kSub);
+    if (e != cudaSuccess) return e;
+    p.tblocks = P::kSub < p.nb ? P::kSub : p.nb;
+    if constexpr (P::G::kTable) e = make_table_map(&maps.t, p.T, p.N, p.nb, p.tblocks);
+    else maps.t = maps.w;   // unused
+    if (e != cudaSuccess) return e;
+    if constexpr (EPI == EPI_ACC) return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
     switch (c_dtype) {
-        case DT_F32: return launch_k<WF, BF, EPI, DT_F32>(maps, p, s);
-        case DT_F16: return launch_k<WF, BF, EPI, DT_F16>(maps, p, s);
-        default: return launch_k<WF, BF, EPI, DT_BF16>(maps, p, s);
+        case DT_F32: return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
+        case DT_F16: return launch_k<WF, BF, EPI, DT_F16, BN>(maps, p, s);
+        default: return launch_k<WF, BF, EPI, DT_BF16, BN>(maps, p, s);
+    }
+}
+
+template <int WF, bool BF, int EPI>
+cudaError_t launch_wf(const Maps& maps, const Params& p, int c_dtype, cudaStream_t s) {
+    switch (p.BN) {
+        case 64: return launch_bn<WF, BF, EPI, 64>(maps, p, c_dtype, s);
+        case 128: return launch_bn<WF, BF, EPI, 128>(maps, p, c_dtype, s);
+        default: return launch_bn<WF, BF, EPI, 256>(maps, p, c_dtype, s);
     }
 }
 
@@ -697,6 +769,19 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
     return e;
 }
 
+int prefill_splits(int M, int K, int N, int fmt) {
+    (void)fmt;
+    // Mid-sized M leaves most SMs idle (one block per 128 channels x BN rows): split K across
+    // up to one wave of blocks, each split keeping at least kMinStages stages of 64.
+    constexpr int kMinStages = 8;
+    const int bn = pf::pick_bn(M);
+    const long long tiles = (long long)((N + pf::kBM - 1) / pf::kBM) * ((M + bn - 1) / bn);
+    long long splits = kTargetSms / tiles;
+    const int by_k = (K / pf::kBK) / kMinStages;
+    if (splits > by_k) splits = by_k;
+    return splits > 1 ? (int)splits : 1;
+}
+
 bool prefill_supported(int M, int K, int N, int fmt, int a_dtype) {
     (void)K;
     (void)N;
@@ -709,24 +794,27 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.block; p.nb = a.K / a.block;
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
+    p.splits = a.splits > 1 ? a.splits : 1;
+    // with K-splits the kernel writes float32 partial sums [splits][M][N], reduced in fixed order
+    const int kdt = p.splits > 1 ? DT_F32 : a.c_dtype;
+    if (p.splits > 1) p.C = a.partial;
     const bool bf = a.a_dtype == DT_BF16;
-    const int wf = a.fmt == FMT_INT4 ? pf::WF_INT4 : (a.fmt == FMT_INT8 ? pf::WF_INT8 : pf::WF_FLOAT);
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.A, bf, a.M, a.K, p.BN);
-    if (e == cudaSuccess) e = pf::make_wmap(&maps.w, a.Bp, wf, bf, a.N, a.K);
-    if (e == cudaSuccess) e = wf == pf::WF_FLOAT ? cudaSuccess : pf::make_table_map(&maps.t, a.T, a.N, p.nb);
     if (e != cudaSuccess) return e;
-    if (wf == pf::WF_FLOAT) maps.t = maps.w;   // unused
-    p.c_tma = pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN) ? 1 : 0;
+    p.c_tma = pf::make_out_map(&maps.c, p.C, kdt, a.M, a.N, p.BN, p.splits) ? 1 : 0;
     if (!p.c_tma) maps.c = maps.a;             // unused
     if (a.fmt == FMT_INT4)
-        return bf ? pf::launch_cdt<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
-    if (a.fmt == FMT_INT8)
-        return bf ? pf::launch_cdt<pf::WF_INT8, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
-                  : pf::launch_cdt<pf::WF_INT8, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
-    return bf ? pf::launch_cdt<pf::WF_FLOAT, true, pf::EPI_STORE>(maps, p, a.c_dtype, s)
-              : pf::launch_cdt<pf::WF_FLOAT, false, pf::EPI_STORE>(maps, p, a.c_dtype, s);
+        e = bf ? pf::launch_wf<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, kdt, s)
+               : pf::launch_wf<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, kdt, s);
+    else if (a.fmt == FMT_INT8)
+        e = bf ? pf::launch_wf<pf::WF_INT8, true, pf::EPI_STORE>(maps, p, kdt, s)
+               : pf::launch_wf<pf::WF_INT8, false, pf::EPI_STORE>(maps, p, kdt, s);
+    else
+        e = bf ? pf::launch_wf<pf::WF_FLOAT, true, pf::EPI_STORE>(maps, p, kdt, s)
+               : pf::launch_wf<pf::WF_FLOAT, false, pf::EPI_STORE>(maps, p, kdt, s);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    return launch_splitk_reduce(a.partial, p.splits, (size_t)a.M * a.N, a.C, a.c_dtype, s);
 }
 
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
@@ -734,17 +822,15 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.K; p.nb = 1;
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
-    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc;
+    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc; p.splits = 1;
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
-    if (e == cudaSuccess) e = pf::make_wmap(&maps.w, a.Bp, pf::WF_CODES4, false, a.N, a.K);
     if (e != cudaSuccess) return e;
-    maps.t = maps.w;   // unused: the per-channel scale is applied in the epilogue
-    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN) ? 1 : 0)
-                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN) ? 1 : 0);
+    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN, 1) ? 1 : 0)
+                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN, 1) ? 1 : 0);
     if (!p.c_tma) maps.c = maps.a;     // unused
-    if (a.acc) return pf::launch_k<pf::WF_CODES4, false, pf::EPI_ACC, DT_F32>(maps, p, s);
-    return pf::launch_cdt<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
+    if (a.acc) return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_ACC>(maps, p, DT_F32, s);
+    return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s) {

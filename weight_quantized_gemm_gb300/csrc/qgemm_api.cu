@@ -14,6 +14,7 @@ namespace {
 thread_local char g_last_error[256] = "";
 std::atomic<int> g_opt_overlap{0};
 std::atomic<int> g_opt_decode_max_m{16};
+std::atomic<int> g_opt_split_k{1};
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -59,23 +60,44 @@ size_t packed_bytes(int K, int N, int mode, int w_dtype) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t w4a8_ws(int M, int K) { return align256((size_t)M * K * 2) + align256((size_t)M * 4) * 2; }
 
+int fmt_of(int mode) {
+    return mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
+}
+
 // Kernel choice by shape (one backend: these are all this library's CUDA kernels).
 enum Path { PATH_F32, PATH_DECODE, PATH_PREFILL };
 Path choose_path(int M, int K, int N, int mode, int a_dtype) {
     if (a_dtype == QGEMM_F32) return PATH_F32;
-    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
-    if (M > g_opt_decode_max_m.load(std::memory_order_relaxed) && qg::prefill_supported(M, K, N, fmt, a_dtype))
+    if (M > g_opt_decode_max_m.load(std::memory_order_relaxed) && qg::prefill_supported(M, K, N, fmt_of(mode), a_dtype))
         return PATH_PREFILL;
     return PATH_DECODE;
 }
 
-size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype) {
+// K-splits of the tensor-core path for this call: the shape's choice, lowered until the float32
+// partial sums [splits][M][N] fit in ws_bytes of scratch.
+int prefill_splits_for(int M, int K, int N, int mode, size_t ws_bytes) {
+    if (!g_opt_split_k.load(std::memory_order_relaxed)) return 1;
+    int splits = qg::prefill_splits(M, K, N, fmt_of(mode));
+    const size_t per = (size_t)M * N * sizeof(float);
+    while (splits > 1 && (size_t)splits * per > ws_bytes) --splits;
+    return splits;
+}
+
+// Scratch bytes of a call. The decode split-K partials and the W4A8 codes are required; the
+// tensor-core path's split-K partials are optional (with less scratch it splits less), so
+// `required` leaves them out.
+size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool required) {
     if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K);
-    if (choose_path(M, K, N, mode, a_dtype) != PATH_DECODE) return 0;
+    const Path path = choose_path(M, K, N, mode, a_dtype);
+    if (path == PATH_PREFILL) {
+        if (required) return 0;
+        const int splits = prefill_splits_for(M, K, N, mode, SIZE_MAX);
+        return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    }
+    if (path != PATH_DECODE) return 0;
     // the decode kernel runs 16 rows of A at a time; split-K partials are per 16-row launch
     const int mc = M < 16 ? M : 16;
-    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
-    const int splits = qg::decode_splits(mc, K, N, fmt, block == 0 ? K : block);
+    const int splits = qg::decode_splits(mc, K, N, fmt_of(mode), block == 0 ? K : block);
     return splits > 1 ? (size_t)splits * mc * N * sizeof(float) : 0;
 }
 
@@ -94,12 +116,17 @@ int qgemm_set_option(int option, int value) {
         if (value < 16 || value > 1024) return fail(QGEMM_ERR_ARG, "option %d takes 16..1024, got %d", option, value);
         return g_opt_decode_max_m.exchange(value);
     }
+    if (option == QGEMM_OPT_SPLIT_K) {
+        if (value != 0 && value != 1) return fail(QGEMM_ERR_ARG, "option %d takes 0 or 1, got %d", option, value);
+        return g_opt_split_k.exchange(value);
+    }
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
 int qgemm_get_option(int option) {
     if (option == QGEMM_OPT_LAUNCH_OVERLAP) return g_opt_overlap.load();
     if (option == QGEMM_OPT_DECODE_MAX_M) return g_opt_decode_max_m.load();
+    if (option == QGEMM_OPT_SPLIT_K) return g_opt_split_k.load();
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
@@ -118,7 +145,7 @@ size_t qgemm_table_bytes(int K, int N, int mode, int block) {
 size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype) {
     if (M <= 0 || check_shape(K, N, mode, &block) != QGEMM_OK || !valid_dtype(a_dtype) || !valid_dtype(c_dtype))
         return 0;
-    return run_ws(M, K, N, mode, block, a_dtype);
+    return run_ws(M, K, N, mode, block, a_dtype, false);
 }
 
 int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, void* Bp, float* T, void* stream) {
@@ -155,7 +182,7 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
         (workspace && !aligned16(workspace)))
         return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C and workspace must be 16-byte aligned");
     if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
-    const size_t need = run_ws(M, K, N, mode, block, a_dtype);
+    const size_t need = run_ws(M, K, N, mode, block, a_dtype, true);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
@@ -173,10 +200,11 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
     }
 
-    const int fmt = mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
+    const int fmt = fmt_of(mode);
     const Path path = choose_path(M, K, N, mode, a_dtype);
     if (path == PATH_PREFILL) {
-        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C};
+        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C, static_cast<float*>(workspace), 1};
+        pa.splits = prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes : 0);
         e = qg::launch_prefill(pa, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
     }
@@ -291,7 +319,7 @@ int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, i
     if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
         return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
     if (M == 0 || N == 0) return QGEMM_OK;
-    const size_t need = run_ws(M, K, N, mode, blk, a_dtype);
+    const size_t need = run_ws(M, K, N, mode, blk, a_dtype, true);
     if (need > QGEMM_NOALLOC_SCRATCH_BYTES)
         return fail(QGEMM_ERR_WORKSPACE, "this call needs %zu bytes of scratch; the built-in scratch holds %u", need,
                     QGEMM_NOALLOC_SCRATCH_BYTES);
