@@ -120,6 +120,30 @@ int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, v
 int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
               const float* T, void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- fused epilogue */
+
+/* Activations of qgemm_run_fused. */
+#define QGEMM_ACT_NONE 0
+#define QGEMM_ACT_RELU 1        /* max(x, 0) */
+#define QGEMM_ACT_SILU 2        /* x / (1 + exp(-x)) */
+#define QGEMM_ACT_GELU_TANH 3   /* 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3))) */
+
+/* qgemm_run with the layer's neighbours fused into its output store. The pull request
+ * "vulkan: 在骁龙 8 Gen 3（Adreno 750，安卓）上跑通并调优无协作矩阵档" keeps the float32 accumulators
+ * until bias, residual and activation are applied (note on the DIRECT build); here
+ *   C[m][n] = act(acc[m][n] + bias[n]) + residual[m][n]
+ * in float32, rounded once to c_dtype, where acc is what qgemm_run would round (for W4A8 the
+ * rescaled result).
+ *   bias: float32 [N], 16-byte aligned, or NULL for none.
+ *   act: QGEMM_ACT_*.
+ *   residual: [M][N] in c_dtype, 16-byte aligned, or NULL for none. It may be C itself (an
+ *   in-place residual add: every element is read before it is written, by the same thread),
+ *   but must not overlap C in any other way.
+ * Kernels, workspace and errors as qgemm_run; an unknown act gives QGEMM_ERR_ARG. */
+int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                    const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* The W4A8 activation step alone (same page and section: "激活动态量化为 INT8"): per row of
  * A [M][K], as[m] = max|a| / 127 (float32), qa = clamp(rint(a / as), -127, 127) with ties
  * to even (all 0 when as == 0), rowsum[m] = sum_k qa. Outputs qa int8 [M][K], as float32 [M],

@@ -69,6 +69,7 @@ def _load():
             "orc_w4a8_acc": [I64, I64, I64, P, P, P],
             "orc_w4a8_acc_points": [I64, P, P, I64, P, P, P],
             "orc_w4a8_out": [I64, I64, P, P, P, P, P],
+            "orc_epilogue": [I64, I64, P, P, I, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -235,6 +236,22 @@ def w4a8_out(acc: np.ndarray, s: np.ndarray, rowsum: np.ndarray, T: np.ndarray) 
     R = np.empty((M, N), dtype=np.float64)
     _check(_load().orc_w4a8_out(M, N, _p(acc), _p(s), _p(rowsum), _p(T), _p(R)), "w4a8_out")
     return R
+
+
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH = 0, 1, 2, 3
+
+
+def epilogue(R: np.ndarray, bias=None, act: int = ACT_NONE, residual=None) -> np.ndarray:
+    """act(R + bias) + residual in float64 (a new array). bias: float32 [N]; residual: the
+    residual's values (float64-convertible) [M][N]. Reading of the Adreno 750 pull request's
+    "before bias, residual and activation": activation first, then the residual."""
+    out = np.array(R, dtype=np.float64, order="C", copy=True)
+    M, N = out.shape
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    r = None if residual is None else np.ascontiguousarray(residual, dtype=np.float64)
+    _check(_load().orc_epilogue(M, N, _p(out), None if b is None else _p(b), act, None if r is None else _p(r)),
+           "epilogue")
+    return out
 
 
 # ---------------------------------------------------------------- whole layer

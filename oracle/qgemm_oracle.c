@@ -303,3 +303,37 @@ int orc_w4a8_out(int64_t M, int64_t N, const int32_t* acc, const float* as, cons
         }
     return ORC_OK;
 }
+
+/*
+ * Output epilogue (the pull request "vulkan: 在骁龙 8 Gen 3（Adreno 750，安卓）上跑通并调优无协作矩阵档"
+ * keeps accumulators unrounded until bias, residual and activation are applied; the order
+ * and the activations are this library's reading): in double, for every output,
+ *   R[m][n] = act(R[m][n] + bias[n]) + residual[m][n]
+ * with act 0 = identity, 1 = max(x, 0), 2 = x * sigmoid(x), 3 = the tanh form of GELU,
+ * 0.5 x (1 + tanh(sqrt(2 / pi) (x + 0.044715 x^3))). bias and residual may be NULL.
+ */
+static double orc_act(int act, double x) {
+    switch (act) {
+        case 1: return x > 0.0 ? x : 0.0;
+        case 2: return x / (1.0 + exp(-x));
+        case 3: {
+            const double c = sqrt(2.0 / 3.14159265358979323846);
+            return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+        }
+        default: return x;
+    }
+}
+
+int orc_epilogue(int64_t M, int64_t N, double* R, const float* bias, int act, const double* residual) {
+    if (!R || M <= 0 || N <= 0 || act < 0 || act > 3) return ORC_ERR_ARG;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double v = R[m * N + n];
+            if (bias) v += (double)bias[n];
+            v = orc_act(act, v);
+            if (residual) v += residual[m * N + n];
+            R[m * N + n] = v;
+        }
+    return ORC_OK;
+}

@@ -128,3 +128,15 @@ def test_error_strings():
     for code, name in qg.ERRORS.items():
         assert qg.qgemm_error_string(code) == name
     assert qg.qgemm_error_string(0) == "QGEMM_OK"
+
+
+def test_fused_epilogue_argument_checks():
+    """qgemm_run_fused validates its epilogue before anything is launched."""
+    lib = qg.load()
+    FAKE = 1 << 20
+    run = lib.qgemm_run_fused
+    assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, None, 9, None, FAKE, 2, None, 0, None) == -1      # unknown act
+    assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, None, -1, None, FAKE, 2, None, 0, None) == -1
+    assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, FAKE + 4, 0, None, FAKE, 2, None, 0, None) == -3  # bias
+    assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, None, 0, FAKE + 2, FAKE, 2, None, 0, None) == -3  # residual
+    assert run(0, 128, 8, 1, 64, None, 2, None, None, None, 3, None, None, 2, None, 0, None) == 0      # empty call

@@ -260,3 +260,34 @@ def test_flop_convention_reproduces_page():
         assert lo <= float(g) <= hi, (label, lo, g, hi)
         # a different convention (1*M*K*N, or 1e9 in place of 1e6 per ms) misses by 2x / 1000x
         assert not (lo <= 2 * float(g) <= hi)
+
+
+# ------------------------------------------------------------------ output epilogue
+def test_epilogue_pins():
+    """act(R + bias) + residual (Adreno 750 pull request: accumulators kept until bias, residual
+    and activation). Each activation against an independent routine or identity, bias and
+    residual as exact adds, and the reading of the order (activation before the residual)."""
+    sp = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(7)
+    R = rng.normal(0.0, 3.0, (9, 33))
+    bias = rng.normal(0.0, 1.0, 33).astype(np.float32)
+    res = rng.normal(0.0, 1.0, (9, 33))
+    x = R + bias.astype(np.float64)
+    assert np.array_equal(oracle.epilogue(R), R)
+    assert np.array_equal(oracle.epilogue(R, bias, oracle.ACT_NONE, res), x + res)
+    assert np.array_equal(oracle.epilogue(R, bias, oracle.ACT_RELU), np.maximum(x, 0.0))
+    # SiLU against scipy's logistic function
+    np.testing.assert_allclose(oracle.epilogue(R, bias, oracle.ACT_SILU), x * sp.expit(x), rtol=1e-14, atol=1e-300)
+    # tanh-form GELU: g(x) - g(-x) = x exactly (the tanh part is odd), g(0) = 0, and within the
+    # form's known 4.8e-4 of the exact x * Phi(x); a wrong constant (0.04 for 0.044715,
+    # sqrt(pi/2) or 2/pi for sqrt(2/pi)) or a dropped cube misses that bound by 6x or more
+    t = np.linspace(-8.0, 8.0, 4001).reshape(1, -1)
+    g = oracle.epilogue(t, None, oracle.ACT_GELU_TANH)
+    gm = oracle.epilogue(-t, None, oracle.ACT_GELU_TANH)
+    np.testing.assert_allclose(g - gm, t, rtol=0, atol=1e-13)
+    assert oracle.epilogue(np.zeros((1, 1)), None, oracle.ACT_GELU_TANH)[0, 0] == 0.0
+    assert np.abs(g - t * sp.ndtr(t)).max() < 5e-4
+    # the order: ReLU(-2) + 5 = 5 (not ReLU(-2 + 5) = 3)
+    assert oracle.epilogue(np.full((1, 1), -2.0), None, oracle.ACT_RELU, np.full((1, 1), 5.0))[0, 0] == 5.0
+    with pytest.raises(ValueError):
+        oracle.epilogue(R, None, 7)

@@ -15,7 +15,7 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_fused", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
@@ -23,6 +23,7 @@ MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
 OPT_LAUNCH_OVERLAP = 1
 OPT_DECODE_MAX_M = 2
 OPT_SPLIT_K = 3
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 4 << 20
 F32, F16, BF16 = 0, 1, 2
 OK = 0
@@ -40,6 +41,7 @@ SIGNATURES = {
     "qgemm_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
     "qgemm_pack": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "qgemm_run": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _SZ, _P], _I),
+    "qgemm_run_fused": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P, _SZ, _P], _I),
     "qgemm_act_quant": ([_I, _I, _P, _I, _P, _P, _P, _P], _I),
     "qgemm_w4a8_acc": ([_I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
     "qgemm_w4a8_acc_workspace_bytes": ([_I, _I], _SZ),
@@ -121,6 +123,16 @@ def qgemm_run(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp
         workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().qgemm_run(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(C), c_dtype,
                             _ptr(workspace), workspace_bytes, _stream(stream)), "qgemm_run")
+
+
+def qgemm_run_fused(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, bias, act: int, residual,
+                    C, c_dtype: int, workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    """C = act(A x dequant(Bp, T) + bias) + residual (see qgemm.h); bias / residual may be None."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().qgemm_run_fused(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(bias), act,
+                                  _ptr(residual), _ptr(C), c_dtype, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qgemm_run_fused")
 
 
 def qgemm_run_noalloc(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, C, c_dtype: int,

@@ -18,11 +18,12 @@ using dec::store_out;
 using dec::Share;
 
 template <int CDT>
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, size_t count, void* C) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, size_t count, int N, Epilogue ep,
+                                     void* C) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
         float s = 0.f;
         for (int y = 0; y < splits; ++y) s += partial[(size_t)y * count + i];
-        store_out<CDT>(C, i, s);
+        store_out<CDT>(C, i, epilogue_apply<CDT>(ep, s, i, (int)(i % (size_t)N)));
     }
 }
 
@@ -88,7 +89,10 @@ __global__ void __launch_bounds__(256) decode_f32_kernel(DecodeArgs p) {
     if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kRowsM; ++r)
-            if (m0 + r < p.M) store_out<CDT>(p.C, (size_t)(m0 + r) * p.N + n, acc[r]);
+            if (m0 + r < p.M) {
+                const size_t mn = (size_t)(m0 + r) * p.N + n;
+                store_out<CDT>(p.C, mn, epilogue_apply<CDT>(p.ep, acc[r], mn, n));
+            }
     }
     }
 }
@@ -140,27 +144,28 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
         c.M = a.M - m0 < 16 ? a.M - m0 : 16;
         c.A = static_cast<const uint8_t*>(a.A) + (size_t)m0 * a.K * esz;
         c.C = static_cast<uint8_t*>(a.C) + (size_t)m0 * a.N * csz;
+        if (a.ep.residual) c.ep.residual = static_cast<const uint8_t*>(a.ep.residual) + (size_t)m0 * a.N * csz;
         c.splits = decode_splits(c.M, a.K, a.N, a.fmt, a.block);
         cudaError_t e = launch_one(c, s);
         if (e != cudaSuccess || c.splits <= 1) {
             if (e != cudaSuccess) return e;
             continue;
         }
-        e = launch_splitk_reduce(c.partial, c.splits, (size_t)c.M * c.N, c.C, c.c_dtype, s);
+        e = launch_splitk_reduce(c.partial, c.splits, (size_t)c.M * c.N, c.N, c.ep, c.C, c.c_dtype, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, void* C, int c_dtype,
-                                 cudaStream_t s) {
+cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, int N, const Epilogue& ep, void* C,
+                                 int c_dtype, cudaStream_t s) {
     const int threads = 256;
     const size_t want = (count + threads - 1) / threads;
     const int blocks = (int)(want < 4096 ? want : 4096);
     switch (c_dtype) {
-        case DT_F32: splitk_reduce_kernel<DT_F32><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
-        case DT_F16: splitk_reduce_kernel<DT_F16><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
-        default: splitk_reduce_kernel<DT_BF16><<<blocks, threads, 0, s>>>(partial, splits, count, C); break;
+        case DT_F32: splitk_reduce_kernel<DT_F32><<<blocks, threads, 0, s>>>(partial, splits, count, N, ep, C); break;
+        case DT_F16: splitk_reduce_kernel<DT_F16><<<blocks, threads, 0, s>>>(partial, splits, count, N, ep, C); break;
+        default: splitk_reduce_kernel<DT_BF16><<<blocks, threads, 0, s>>>(partial, splits, count, N, ep, C); break;
     }
     return cudaGetLastError();
 }

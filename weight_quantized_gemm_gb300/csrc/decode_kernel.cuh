@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace qg {
@@ -653,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
                 if (gridDim.y > 1)
                     p.partial[((size_t)blockIdx.y * M + m) * N + row] = s;
                 else
-                    store_out<CDT>(p.C, (size_t)m * N + row, s);
+                    store_out<CDT>(p.C, (size_t)m * N + row, epilogue_apply<CDT>(p.ep, s, (size_t)m * N + row, row));
             }
         }
     }

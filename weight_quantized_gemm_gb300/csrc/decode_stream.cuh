@@ -94,6 +94,7 @@ struct Params {
     void* C;
     float* partial;     // [splits][M][N] when gridDim.y > 1
     unsigned int* status;
+    Epilogue ep;        // applied to the final sums (not to split partials)
 };
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
                 if (gridDim.y > 1)
                     p.partial[((size_t)blockIdx.y * p.M + m) * p.N + row] = sum;
                 else
-                    store_out<CDT>(p.C, (size_t)m * p.N + row, sum);
+                    store_out<CDT>(p.C, (size_t)m * p.N + row, epilogue_apply<CDT>(p.ep, sum, (size_t)m * p.N + row, row));
             }
         }
         consumer_sync();
@@ -529,6 +530,7 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     plan.p.T = a.T;
     plan.p.C = a.C;
     plan.p.partial = a.partial;
+    plan.p.ep = a.ep;
     plan.p.status = status_word_address();
     if (!plan.p.status) return cudaErrorInvalidValue;
     CUtensorMap wmap;

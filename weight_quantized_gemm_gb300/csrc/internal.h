@@ -13,6 +13,16 @@ enum Dt { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2 };
 
 inline size_t dt_size(int dt) { return dt == DT_F32 ? 4 : 2; }
 
+// Output epilogue (epilogue.cuh): C = act(acc + bias) + residual, applied in float32 before the
+// one rounding to C's type. The activation codes are the C ABI's QGEMM_ACT_* values.
+enum Act { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2, ACT_GELU_TANH = 3 };
+struct Epilogue {
+    const float* bias = nullptr;        // [N] float32, or none
+    const void* residual = nullptr;     // [M][N] in C's type, or none (may be C itself)
+    int act = ACT_NONE;
+    __host__ __device__ bool any() const { return bias || residual || act != ACT_NONE; }
+};
+
 // The {offset, scale} table T holds one float32 pair per (output channel n, K-block b), stored in
 // groups of 16 channels: [ceil(N / 16)][nb][16][2]. The entries of a 16-channel group for a run
 // of K-blocks are then one contiguous, 128-byte aligned range (one bulk copy), and the 16
@@ -46,15 +56,16 @@ struct DecodeArgs {
     float* partial;   // [splits][M][N] f32 partial sums when splits > 1
     int splits;       // number of K-splits across thread blocks (>= 1)
     int overlap;      // launch with a programmatic dependency on the previous kernel
+    Epilogue ep;
 };
 // K-splits the decode kernels use for this shape, at most 16 rows of A (1 = none); block is the
 // table's K-group (K for per-channel).
 int decode_splits(int M, int K, int N, int fmt, int block);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-// C[i] = sum over y = 0 .. splits-1, in that order, of partial[y * count + i] (float32), rounded
-// once to c_dtype.
-cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, void* C, int c_dtype,
-                                 cudaStream_t s);
+// C[i] = epilogue(sum over y = 0 .. splits-1, in that order, of partial[y * count + i]) (float32),
+// rounded once to c_dtype; i = m * N + n.
+cudaError_t launch_splitk_reduce(const float* partial, int splits, size_t count, int N, const Epilogue& ep, void* C,
+                                 int c_dtype, cudaStream_t s);
 // Exact float32 CUDA-core kernel (any activation dtype, any M); used for f32 activations.
 cudaError_t launch_decode_f32(const DecodeArgs& a, cudaStream_t s);
 
@@ -67,6 +78,7 @@ struct PrefillArgs {
     void* C;
     float* partial;   // [splits][M][N] f32 partial sums when splits > 1
     int splits;       // K-splits across thread blocks (>= 1), from prefill_splits
+    Epilogue ep;
 };
 // K-splits the tensor-core kernel uses for this shape (1 = none); host-only, no GPU needed.
 int prefill_splits(int M, int K, int N, int fmt);
@@ -89,6 +101,7 @@ struct W4A8Args {
     int32_t* acc;   // int32 accumulators out (or nullptr)
     void* C;        // rescaled output (or nullptr)
     int c_dtype;
+    Epilogue ep;    // applied to the rescaled output
 };
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
 

@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -63,6 +64,7 @@ struct Params {
     int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
     int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
     int tblocks;              // K-blocks per table box (min(SUB, nb))
+    Epilogue ep;              // bias / activation / residual (none when the output is split partials)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -522,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         constexpr int kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2;
         uint8_t* tile = smem;
         if (ok) {
+            const bool has_ep = p.ep.any();
             float ws = 0.f, wo = 0.f;
             if constexpr (EPI == EPI_W4A8) {
                 const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
@@ -539,13 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     const size_t t = (size_t)ml * kBM + r;
                     if constexpr (EPI == EPI_ACC) {
                         reinterpret_cast<int32_t*>(tile)[t] = __float2int_rn(d);
-                    } else if constexpr (EPI == EPI_W4A8) {
-                        // d is the exact integer accumulator (see the file comment):
-                        // as * (ws * d + wo * rowsum) = ws * (as * d) + wo * (as * rowsum)
-                        const float2 f = rowf[ml];   // the same row for the whole warp: a broadcast
-                        store_c<CDT>(tile, t, fmaf(ws, f.x * d, wo * f.y));
                     } else {
-                        store_c<CDT>(tile, t, d);
+                        float y = d;
+                        if constexpr (EPI == EPI_W4A8) {
+                            // d is the exact integer accumulator (see the file comment):
+                            // as * (ws * d + wo * rowsum) = ws * (as * d) + wo * (as * rowsum)
+                            const float2 f = rowf[ml];   // the same row for the whole warp: a broadcast
+                            y = fmaf(ws, f.x * d, wo * f.y);
+                        }
+                        if (has_ep && row < p.N && m_tile + ml < p.M)
+                            y = epilogue_apply<CDT>(p.ep, y, (size_t)(m_tile + ml) * p.N + row, row);
+                        store_c<CDT>(tile, t, y);
                     }
                 }
             }
@@ -795,6 +802,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.splits = a.splits > 1 ? a.splits : 1;
+    p.ep = p.splits > 1 ? Epilogue{} : a.ep;   // split partials: the reduction applies it
     // with K-splits the kernel writes float32 partial sums [splits][M][N], reduced in fixed order
     const int kdt = p.splits > 1 ? DT_F32 : a.c_dtype;
     if (p.splits > 1) p.C = a.partial;
@@ -814,7 +822,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
         e = bf ? pf::launch_wf<pf::WF_FLOAT, true, pf::EPI_STORE>(maps, p, kdt, s)
                : pf::launch_wf<pf::WF_FLOAT, false, pf::EPI_STORE>(maps, p, kdt, s);
     if (e != cudaSuccess || p.splits == 1) return e;
-    return launch_splitk_reduce(a.partial, p.splits, (size_t)a.M * a.N, a.C, a.c_dtype, s);
+    return launch_splitk_reduce(a.partial, p.splits, (size_t)a.M * a.N, a.N, a.ep, a.C, a.c_dtype, s);
 }
 
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
@@ -823,6 +831,7 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc; p.splits = 1;
+    p.ep = a.acc ? Epilogue{} : a.ep;
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
     if (e != cudaSuccess) return e;

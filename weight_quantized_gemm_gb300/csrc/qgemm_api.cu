@@ -170,17 +170,25 @@ int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, v
 
 int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp, const float* T,
               void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    return qgemm_run_fused(M, K, N, mode, block, A, a_dtype, Bp, T, nullptr, QGEMM_ACT_NONE, nullptr, C, c_dtype,
+                           workspace, workspace_bytes, stream);
+}
+
+int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                    const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
     int rc = check_shape(K, N, mode, &block);
     if (rc != QGEMM_OK) return rc;
     if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
     if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
         return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
+    if (act < QGEMM_ACT_NONE || act > QGEMM_ACT_GELU_TANH) return fail(QGEMM_ERR_ARG, "unknown activation %d", act);
     if (M == 0 || N == 0) return QGEMM_OK;
     if (!A || !Bp || !C) return fail(QGEMM_ERR_ARG, "null A, Bp or C");
     if (mode != QGEMM_MODE_FLOAT && !T) return fail(QGEMM_ERR_ARG, "null T");
     if (!aligned16(A) || !aligned16(Bp) || !aligned16(C) || (T && !aligned16(T)) ||
-        (workspace && !aligned16(workspace)))
-        return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C and workspace must be 16-byte aligned");
+        (workspace && !aligned16(workspace)) || (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
+        return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C, bias, residual and workspace must be 16-byte aligned");
     if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
     const size_t need = run_ws(M, K, N, mode, block, a_dtype, true);
     if (need > 0 && (!workspace || workspace_bytes < need))
@@ -188,6 +196,10 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
                     workspace ? workspace_bytes : (size_t)0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    qg::Epilogue ep;
+    ep.bias = bias;
+    ep.residual = residual;
+    ep.act = act;
 
     if (mode == QGEMM_MODE_W4A8) {
         void* qa16 = workspace;
@@ -195,7 +207,7 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
         int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
         e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
         if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype};
+        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep};
         e = qg::launch_w4a8_gemm(w, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
     }
@@ -203,7 +215,7 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
     const int fmt = fmt_of(mode);
     const Path path = choose_path(M, K, N, mode, a_dtype);
     if (path == PATH_PREFILL) {
-        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C, static_cast<float*>(workspace), 1};
+        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C, static_cast<float*>(workspace), 1, ep};
         pa.splits = prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes : 0);
         e = qg::launch_prefill(pa, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
@@ -212,6 +224,7 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
     da.M = M; da.K = K; da.N = N; da.block = block; da.fmt = fmt;
     da.a_dtype = a_dtype; da.c_dtype = c_dtype;
     da.A = A; da.Bp = Bp; da.T = T; da.C = C;
+    da.ep = ep;
     if (path == PATH_F32) {
         da.splits = 1;
         e = qg::launch_decode_f32(da, s);
