@@ -45,9 +45,11 @@ DTYPE_NAME = {0: "f32", 1: "f16", 2: "bf16"}
 
 
 # ---------------------------------------------------------------- workload accounting
-def algorithmic_bytes(w: synth.Workload) -> int:
-    """Bytes one call must move: packed weights + table + activations in + output out."""
+def algorithmic_bytes(w: synth.Workload, bias: bool = False, residual: bool = False) -> int:
+    """Bytes one call must move: packed weights + table + activations in + output out (+ the
+    fused epilogue's bias and residual reads)."""
     esz = {0: 4, 1: 2, 2: 2}
+    extra = (w.N * 4 if bias else 0) + (w.M * w.N * esz[w.c_dtype] if residual else 0)
     if w.mode == synth.MODE_FLOAT:
         wb = w.K * w.N * esz[w.a_dtype]
         tb = 0
@@ -55,7 +57,7 @@ def algorithmic_bytes(w: synth.Workload) -> int:
         wb = w.K * w.N * (4 if w.mode in (synth.MODE_INT4, synth.MODE_W4A8) else 8) // 8
         blk = w.K if (w.block == 0 or w.mode == synth.MODE_W4A8) else w.block
         tb = w.N * (w.K // blk) * 8
-    return wb + tb + w.M * w.K * esz[w.a_dtype] + w.M * w.N * esz[w.c_dtype]
+    return wb + tb + w.M * w.K * esz[w.a_dtype] + w.M * w.N * esz[w.c_dtype] + extra
 
 
 def bound_of(w: synth.Workload) -> str:
@@ -244,6 +246,9 @@ def to_torch(arr: np.ndarray, code: int, device):
     return t.to(device)
 
 
+ACTS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+
+
 def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
     import torch
 
@@ -279,18 +284,39 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
         C = torch.empty((M, N), dtype=tdt[w.c_dtype], device=device)
         wsb = qg.qgemm_workspace_bytes(M, K, N, w.mode, w.block, w.a_dtype, w.c_dtype)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+        # the fused epilogue's inputs (qgemm_run_fused), when asked for
+        bias = (torch.from_numpy(synth.normal64(N, 11, stream=4, std=0.5).astype(np.float32)).to(device)
+                if args.bias else None)
+        res = (to_torch(synth.encode(synth.normal64(M * N, 12, stream=5).reshape(M, N), w.c_dtype), w.c_dtype, device)
+               if args.residual else None)
     stream.synchronize()
     s_ptr = stream.cuda_stream
     lib = qg.load()
+    act = ACTS[args.act]
+    fused = bias is not None or res is not None or act != 0
 
     def call(i):
-        rc = lib.qgemm_run(M, K, N, w.mode, w.block, As[i % len(As)].data_ptr(), w.a_dtype, Bps[i % copies].data_ptr(),
-                           Ts[i % copies].data_ptr() if tb else None, C.data_ptr(), w.c_dtype, ws.data_ptr(), wsb,
-                           s_ptr)
+        if fused:
+            rc = lib.qgemm_run_fused(M, K, N, w.mode, w.block, As[i % len(As)].data_ptr(), w.a_dtype,
+                                     Bps[i % copies].data_ptr(), Ts[i % copies].data_ptr() if tb else None,
+                                     None if bias is None else bias.data_ptr(), act,
+                                     None if res is None else res.data_ptr(), C.data_ptr(), w.c_dtype,
+                                     ws.data_ptr(), wsb, s_ptr)
+        else:
+            rc = lib.qgemm_run(M, K, N, w.mode, w.block, As[i % len(As)].data_ptr(), w.a_dtype,
+                               Bps[i % copies].data_ptr(), Ts[i % copies].data_ptr() if tb else None, C.data_ptr(),
+                               w.c_dtype, ws.data_ptr(), wsb, s_ptr)
         if rc != 0:
             raise qg.QgemmError(rc, "qgemm_run")
 
-    launches_per_call = 1 + (1 if (w.mode == synth.MODE_W4A8) else 0)
+    # kernels per call: W4A8 = activation quantization + GEMM; otherwise one GEMM launch per
+    # 16-row decode launch (or one tensor-core launch), plus the split-K reduction when the call
+    # splits K (its workspace holds the partial sums)
+    if w.mode == synth.MODE_W4A8:
+        launches_per_call = 2
+    else:
+        decode_path = w.a_dtype != synth.F32 and M <= (args.decode_max_m or 16)
+        launches_per_call = (-(-M // 16) if decode_path else 1) * (2 if wsb > 0 else 1)
     # warm-up (eager), then one CUDA graph of exactly K calls per launch mode: plain stream
     # order, and with QGEMM_OPT_LAUNCH_OVERLAP (each decode call may start while the previous
     # one finishes; it prefetches weights and waits for the previous kernel before A and C).
@@ -394,6 +420,10 @@ def main():
                     help="QGEMM_OPT_DECODE_MAX_M for the run (the decode / tensor-core crossover)")
     ap.add_argument("--no-split-k", action="store_true",
                     help="QGEMM_OPT_SPLIT_K = 0: the tensor-core kernel never splits K")
+    ap.add_argument("--act", default="none", choices=sorted(ACTS),
+                    help="fused epilogue activation (qgemm_run_fused)")
+    ap.add_argument("--bias", action="store_true", help="fused epilogue: add a float32 bias [N]")
+    ap.add_argument("--residual", action="store_true", help="fused epilogue: add a residual [M][N]")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--print-src-hash", action="store_true", help="print the dominant kernel's source hash and exit")
@@ -417,6 +447,8 @@ def main():
     base_config = {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "mode": synth.MODE_NAMES[w.mode],
                    "block": w.block if w.block else w.K, "a_dtype": DTYPE_NAME[w.a_dtype],
                    "c_dtype": DTYPE_NAME[w.c_dtype]}
+    if args.bias or args.residual or args.act != "none":
+        base_config["epilogue"] = {"bias": args.bias, "act": args.act, "residual": args.residual}
 
     if args.impl == "reference":
         if rank != 0:
@@ -445,7 +477,7 @@ def main():
         dist = dist_mod
     r = run_gpu(args, w, rank, world, dist)
     step_s = r["ms"] / 1e3 / args.steps
-    alg = algorithmic_bytes(w)
+    alg = algorithmic_bytes(w, args.bias, args.residual)
     gbs = job_rate(alg, step_s, world) / 1e9
     tflops = job_rate(w.flops, step_s, world) / 1e12
     bound = bound_of(w)

@@ -23,7 +23,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
         float s = 0.f;
         for (int y = 0; y < splits; ++y) s += partial[(size_t)y * count + i];
-        store_out<CDT>(C, i, epilogue_apply<CDT>(ep, s, i, (int)(i % (size_t)N)));
+        store_out<CDT>(C, i, epilogue_apply<CDT>(ep, s, i, ep.bias ? (int)(i % (size_t)N) : 0));
     }
 }
 

@@ -360,7 +360,7 @@ struct Issuer {
 // the K-range of split blockIdx.y, for at most 8 * NT rows of A.
 //   ONECOL: M == 1, so only MMA column 0 carries data and only it is scaled.
 //   FULL: every warp owns exactly kSbw sub-blocks (the K-range is 16 * kSbw sub-blocks).
-template <int FMT, bool BF, int NT, bool PERCH, int CDT, bool ONECOL, bool FULL>
+template <int FMT, bool BF, int NT, bool PERCH, bool EP, bool ONECOL, bool FULL>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
     using R = Ring<FMT, NT, PERCH>;
     constexpr int D = R::kDepth;
@@ -654,7 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
                 if (gridDim.y > 1)
                     p.partial[((size_t)blockIdx.y * M + m) * N + row] = s;
                 else
-                    store_out<CDT>(p.C, (size_t)m * N + row, epilogue_apply<CDT>(p.ep, s, (size_t)m * N + row, row));
+                {
+                    const size_t mn = (size_t)m * N + row;
+                    if constexpr (EP) s = epilogue_apply_rt(p.ep, s, mn, row, p.c_dtype);
+                    store_out_rt(p.C, mn, s, p.c_dtype);
+                }
             }
         }
     }
@@ -673,13 +677,13 @@ inline int sm_count() {
     return count;
 }
 
-template <int FMT, bool BF, int NT, bool PERCH, int CDT, bool ONECOL, bool FULL>
+template <int FMT, bool BF, int NT, bool PERCH, bool EP, bool ONECOL, bool FULL>
 cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     const int nsb = a.K / 64;
     const int nsbc = (nsb + a.splits - 1) / a.splits;
     const size_t smem = smem_bytes<FMT, NT, PERCH>(nsbc);
     if (smem > kMaxSmem) return cudaErrorInvalidValue;
-    auto kern = decode_kernel<FMT, BF, NT, PERCH, CDT, ONECOL, FULL>;
+    auto kern = decode_kernel<FMT, BF, NT, PERCH, EP, ONECOL, FULL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int groups = (a.N + 15) / 16;
@@ -701,17 +705,12 @@ template <int FMT, bool BF, int NT, bool PERCH, bool ONECOL>
 cudaError_t launch_c(const DecodeArgs& a, cudaStream_t s) {
     // FULL: every split is exactly 16 warps x kSbw sub-blocks
     const bool full = (a.K / 64) == a.splits * Share<NT>::kSbMaxNt;
-    switch (a.splits > 1 ? DT_F32 : a.c_dtype) {
-        case DT_F32:
-            return full ? launch_v<FMT, BF, NT, PERCH, DT_F32, ONECOL, true>(a, s)
-                        : launch_v<FMT, BF, NT, PERCH, DT_F32, ONECOL, false>(a, s);
-        case DT_F16:
-            return full ? launch_v<FMT, BF, NT, PERCH, DT_F16, ONECOL, true>(a, s)
-                        : launch_v<FMT, BF, NT, PERCH, DT_F16, ONECOL, false>(a, s);
-        default:
-            return full ? launch_v<FMT, BF, NT, PERCH, DT_BF16, ONECOL, true>(a, s)
-                        : launch_v<FMT, BF, NT, PERCH, DT_BF16, ONECOL, false>(a, s);
-    }
+    // the fused epilogue gets its own instantiation (EP); split partials never take it
+    if (a.splits == 1 && a.ep.any())
+        return full ? launch_v<FMT, BF, NT, PERCH, true, ONECOL, true>(a, s)
+                    : launch_v<FMT, BF, NT, PERCH, true, ONECOL, false>(a, s);
+    return full ? launch_v<FMT, BF, NT, PERCH, false, ONECOL, true>(a, s)
+                : launch_v<FMT, BF, NT, PERCH, false, ONECOL, false>(a, s);
 }
 
 // Shapes the TMA-fed kernel of decode_stream.cuh does not take: 9 <= M <= 16, or packed rows that

@@ -94,7 +94,8 @@ struct Params {
     void* C;
     float* partial;     // [splits][M][N] when gridDim.y > 1
     unsigned int* status;
-    Epilogue ep;        // applied to the final sums (not to split partials)
+    Epilogue ep;        // applied to the final sums (not to split partials) by the EP kernels
+    int cdt;            // C's type
 };
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
@@ -106,7 +107,7 @@ __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
 }
 
-template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL, int NT>
+template <int FMT, bool BF, bool PERCH, bool EP, bool ONECOL, int NT>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ CUtensorMap wmap, Params p) {
     using G = Geo<FMT>;
     using Bu = Budget<NT>;
@@ -434,7 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
                 if (gridDim.y > 1)
                     p.partial[((size_t)blockIdx.y * p.M + m) * p.N + row] = sum;
                 else
-                    store_out<CDT>(p.C, (size_t)m * p.N + row, epilogue_apply<CDT>(p.ep, sum, (size_t)m * p.N + row, row));
+                {
+                    const size_t mn = (size_t)m * p.N + row;
+                    if constexpr (EP) sum = epilogue_apply_rt(p.ep, sum, mn, row, p.cdt);
+                    store_out_rt(p.C, mn, sum, p.cdt);
+                }
             }
         }
         consumer_sync();
@@ -521,7 +526,7 @@ inline bool supported(const DecodeArgs& a) {
     return stream_takes(a.M, a.K, FMT, a.block);
 }
 
-template <int FMT, bool BF, bool PERCH, int CDT, bool ONECOL, int NT>
+template <int FMT, bool BF, bool PERCH, bool EP, bool ONECOL, int NT>
 cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     Plan plan;
     if (!make_plan<FMT, NT>(a, &plan)) return cudaErrorInvalidValue;
@@ -531,12 +536,13 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     plan.p.C = a.C;
     plan.p.partial = a.partial;
     plan.p.ep = a.ep;
+    plan.p.cdt = a.c_dtype;
     plan.p.status = status_word_address();
     if (!plan.p.status) return cudaErrorInvalidValue;
     CUtensorMap wmap;
     cudaError_t e = make_wmap(&wmap, a.Bp, plan.p.row_bytes, a.N, plan.p.bz);
     if (e != cudaSuccess) return e;
-    auto kern = stream_kernel<FMT, BF, PERCH, CDT, ONECOL, NT>;
+    auto kern = stream_kernel<FMT, BF, PERCH, EP, ONECOL, NT>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return e;
     const int groups = (a.N + kRows - 1) / kRows;
@@ -555,13 +561,12 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, wmap, plan.p);
 }
 
+// The fused epilogue gets its own instantiation (EP), so that the plain store path is unchanged;
+// split partials never take it (the reduction applies it).
 template <int FMT, bool BF, bool PERCH, bool ONECOL, int NT>
 cudaError_t launch_c(const DecodeArgs& a, cudaStream_t s) {
-    switch (a.splits > 1 ? DT_F32 : a.c_dtype) {
-        case DT_F32: return launch_v<FMT, BF, PERCH, DT_F32, ONECOL, NT>(a, s);
-        case DT_F16: return launch_v<FMT, BF, PERCH, DT_F16, ONECOL, NT>(a, s);
-        default: return launch_v<FMT, BF, PERCH, DT_BF16, ONECOL, NT>(a, s);
-    }
+    if (a.splits == 1 && a.ep.any()) return launch_v<FMT, BF, PERCH, true, ONECOL, NT>(a, s);
+    return launch_v<FMT, BF, PERCH, false, ONECOL, NT>(a, s);
 }
 
 // Shapes stream_takes accepts (M <= 16)

@@ -13,17 +13,32 @@
 
 namespace qg {
 
+// The activations use the fast exponential (a few ulp) and the fast divide: the epilogue runs
+// once per output on the few epilogue warps, and the results are rounded to C's type next.
 __device__ __forceinline__ float act_apply(int act, float v) {
     switch (act) {
         case ACT_RELU: return fmaxf(v, 0.f);
-        case ACT_SILU: return v / (1.f + expf(-v));   // v * sigmoid(v)
+        case ACT_SILU: return __fdividef(v, 1.f + __expf(-v));   // v * sigmoid(v)
         case ACT_GELU_TANH: {
-            // tanh form of GELU: 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))
+            // tanh form of GELU, 0.5 v (1 + tanh(u)) with u = sqrt(2/pi) (v + 0.044715 v^3); as
+            // 1 + tanh(u) = 2 - 2 / (1 + e^(2u)), this is v - v / (1 + e^(2u)), whose error is
+            // absolute in v (no cancellation is amplified) and which is exact at both tails
             const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
-            return 0.5f * v * (1.f + tanhf(u));
+            return v - __fdividef(v, 1.f + __expf(2.f * u));
         }
         default: return v;
     }
+}
+
+// The same with the activation fixed at compile time (loops that hoist the choice).
+template <int ACT>
+__device__ __forceinline__ float act_fixed(float v) {
+    if constexpr (ACT == ACT_RELU) return fmaxf(v, 0.f);
+    else if constexpr (ACT == ACT_SILU) return __fdividef(v, 1.f + __expf(-v));
+    else if constexpr (ACT == ACT_GELU_TANH) {
+        const float u = 0.7978845608028654f * fmaf(0.044715f * v, v * v, v);
+        return v - __fdividef(v, 1.f + __expf(2.f * u));
+    } else return v;
 }
 
 template <int CDT>
@@ -39,6 +54,20 @@ __device__ __forceinline__ float epilogue_apply(const Epilogue& e, float v, size
     if (e.bias) v += __ldg(e.bias + n);
     v = act_apply(e.act, v);
     if (e.residual) v += load_c<CDT>(e.residual, mn);
+    return v;
+}
+// Output type chosen at run time (kernels that store one value per output at their very end).
+__device__ __forceinline__ void store_out_rt(void* C, size_t idx, float v, int cdt) {
+    if (cdt == DT_F32) static_cast<float*>(C)[idx] = v;
+    else if (cdt == DT_F16) static_cast<__half*>(C)[idx] = __float2half_rn(v);
+    else static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ float epilogue_apply_rt(const Epilogue& e, float v, size_t mn, int n, int cdt) {
+    if (e.bias) v += __ldg(e.bias + n);
+    v = act_apply(e.act, v);
+    if (e.residual)
+        v += cdt == DT_F32 ? load_c<DT_F32>(e.residual, mn)
+                           : (cdt == DT_F16 ? load_c<DT_F16>(e.residual, mn) : load_c<DT_BF16>(e.residual, mn));
     return v;
 }
 

@@ -524,36 +524,71 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         constexpr int kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2;
         uint8_t* tile = smem;
         if (ok) {
-            const bool has_ep = p.ep.any();
             float ws = 0.f, wo = 0.f;
             if constexpr (EPI == EPI_W4A8) {
                 const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
                 wo = t.x;
                 ws = t.y;
             }
+            // The fused epilogue: this thread's channel bias once, and per 32-column chunk the 32
+            // residual values (32 independent loads, one 64-byte segment of a residual row per
+            // warp each) before any of them is used; the activation is chosen once per chunk.
+            const bool has_ep = EPI != EPI_ACC && p.ep.any();
+            const bool has_res = has_ep && p.ep.residual != nullptr;
+            const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
             for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kAccCol + c0, v);
-                tmem_ld_wait();
+                float rv[32];
+                if (has_res) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int ml = c0 + i;
-                    const float d = __uint_as_float(v[i]);
-                    const size_t t = (size_t)ml * kBM + r;
-                    if constexpr (EPI == EPI_ACC) {
-                        reinterpret_cast<int32_t*>(tile)[t] = __float2int_rn(d);
-                    } else {
-                        float y = d;
-                        if constexpr (EPI == EPI_W4A8) {
-                            // d is the exact integer accumulator (see the file comment):
-                            // as * (ws * d + wo * rowsum) = ws * (as * d) + wo * (as * rowsum)
-                            const float2 f = rowf[ml];   // the same row for the whole warp: a broadcast
-                            y = fmaf(ws, f.x * d, wo * f.y);
-                        }
-                        if (has_ep && row < p.N && m_tile + ml < p.M)
-                            y = epilogue_apply<CDT>(p.ep, y, (size_t)(m_tile + ml) * p.N + row, row);
-                        store_c<CDT>(tile, t, y);
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = m_tile + c0 + i;
+                        rv[i] = (row < p.N && m < p.M) ? load_c<CDT>(p.ep.residual, (size_t)m * p.N + row) : 0.f;
                     }
+                }
+                tmem_ld_wait();
+                if constexpr (EPI == EPI_ACC) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        reinterpret_cast<int32_t*>(tile)[(size_t)(c0 + i) * kBM + r] = __float2int_rn(__uint_as_float(v[i]));
+                } else {
+                    float y[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        y[i] = __uint_as_float(v[i]);
+                        if constexpr (EPI == EPI_W4A8) {
+                            // y is the exact integer accumulator (see the file comment):
+                            // as * (ws * acc + wo * rowsum) = ws * (as * acc) + wo * (as * rowsum)
+                            const float2 f = rowf[c0 + i];   // the same row for the whole warp: a broadcast
+                            y[i] = fmaf(ws, f.x * y[i], wo * f.y);
+                        }
+                    }
+                    if (has_ep) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) y[i] += bias_r;
+                        switch (p.ep.act) {
+                            case ACT_RELU:
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_RELU>(y[i]);
+                                break;
+                            case ACT_SILU:
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_SILU>(y[i]);
+                                break;
+                            case ACT_GELU_TANH:
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_GELU_TANH>(y[i]);
+                                break;
+                            default: break;
+                        }
+                        if (has_res) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) y[i] += rv[i];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) store_c<CDT>(tile, (size_t)(c0 + i) * kBM + r, y[i]);
                 }
             }
         }
