@@ -71,6 +71,7 @@ extern "C" {
 #define QGEMM_ERR_WORKSPACE (-4)   /* workspace smaller than qgemm_workspace_bytes()            */
 #define QGEMM_ERR_CUDA (-5)        /* a CUDA call or launch failed (detail in qgemm_last_error) */
 #define QGEMM_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait (reported by qgemm_status) */
+#define QGEMM_ERR_IO (-7)          /* a weight file could not be read or written, or is corrupt  */
 
 /* ---------------------------------------------------------------- sizes (host only, no GPU needed) */
 
@@ -187,6 +188,31 @@ size_t qgemm_w4a8_acc_workspace_bytes(int M, int K);
  *     race on it and may produce wrong results. Order them on one stream. */
 int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
                       const float* T, void* C, int c_dtype, void* stream);
+
+/* ---------------------------------------------------------------- packed-weight files */
+
+/* One packed layer per file, so that weights are quantized once (qgemm_pack) and later loaded
+ * ready to run: a 64-byte little-endian header {magic "QGEMMW\0\1", version 1, header size 64,
+ * K, N, mode, block, w_dtype, CRC-32 of the payload, Bp bytes, T bytes}, then Bp, then T (none
+ * in FLOAT mode), byte for byte as qgemm_pack wrote them. The pages have no counterpart; this
+ * is a convenience of this library.
+ * on_device: 1 if Bp / T are device pointers (copied through a host staging buffer on `stream`,
+ * synchronously), 0 if they are host pointers (no CUDA call is made). */
+
+/* Writes Bp (qgemm_packed_bytes) and T (qgemm_table_bytes; NULL in FLOAT mode) of the shape to
+ * `path`, replacing the file. QGEMM_ERR_ARG for an invalid shape or null buffer, QGEMM_ERR_IO if
+ * the file cannot be written. */
+int qgemm_save(const char* path, int K, int N, int mode, int block, int w_dtype, const void* Bp, const float* T,
+               int on_device, void* stream);
+
+/* Reads a file's header: the shape and format to pass to qgemm_packed_bytes / qgemm_table_bytes
+ * and qgemm_run. QGEMM_ERR_IO for a missing, foreign or inconsistent file. */
+int qgemm_load_info(const char* path, int* K, int* N, int* mode, int* block, int* w_dtype);
+
+/* Reads a file's Bp and T into buffers of at least the file's sizes (QGEMM_ERR_ARG if smaller).
+ * The whole payload is read and its CRC-32 checked before anything is written to Bp or T:
+ * a truncated, extended or corrupt file gives QGEMM_ERR_IO and leaves them untouched. */
+int qgemm_load(const char* path, void* Bp, size_t Bp_bytes, float* T, size_t T_bytes, int on_device, void* stream);
 
 /* ---------------------------------------------------------------- options */
 

@@ -227,3 +227,27 @@ def test_launch_overlap_chained_layers_bit_identical():
             assert np.array_equal(a, o.float().cpu().numpy())
     finally:
         qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, prev)
+
+
+# ---------------------------------------------------------------- packed-weight files
+@pytest.mark.parametrize("mode,block,M", [(1, 64, 1), (2, 0, 40), (0, 0, 3)])
+def test_weight_file_round_trip_on_device(tmp_path, mode, block, M):
+    """qgemm_save from device buffers, qgemm_load into fresh ones: the same bytes, and the
+    layer run on the loaded weights gives exactly the output of the original ones."""
+    K, N = 512, 200
+    w = synth.Workload("t", M, K, N, mode, block, synth.BF16, synth.BF16, 1, 2)
+    A_np, W_np = synth.make_activations(w), synth.make_weights(w)
+    w_dtype = synth.BF16 if mode == 0 else 0
+    Bp, T = gpu_pack(W_np, mode, block, w_dtype)
+    path = str(tmp_path / "layer.qgw")
+    qg.qgemm_save(path, K, N, mode, block, w_dtype, Bp, T)
+    info = qg.qgemm_load_info(path)
+    assert info == {"K": K, "N": N, "mode": mode, "block": block, "w_dtype": w_dtype}
+    Bp2 = torch.zeros_like(Bp)
+    T2 = None if T is None else torch.zeros_like(T)
+    qg.qgemm_load(path, Bp2, T2)
+    torch.cuda.synchronize()
+    assert torch.equal(Bp2, Bp) and (T is None or torch.equal(T2, T))
+    got1 = gpu_run(M, K, N, mode, block, A_np, synth.BF16, Bp, T, synth.BF16)
+    got2 = gpu_run(M, K, N, mode, block, A_np, synth.BF16, Bp2, T2, synth.BF16)
+    assert np.array_equal(got1, got2)

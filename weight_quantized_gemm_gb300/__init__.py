@@ -15,7 +15,7 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_fused", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_fused", "qgemm_save", "qgemm_load_info", "qgemm_load", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
@@ -28,7 +28,7 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 F32, F16, BF16 = 0, 1, 2
 OK = 0
 ERRORS = {-1: "QGEMM_ERR_ARG", -2: "QGEMM_ERR_UNSUPPORTED", -3: "QGEMM_ERR_ALIGN", -4: "QGEMM_ERR_WORKSPACE",
-          -5: "QGEMM_ERR_CUDA", -6: "QGEMM_ERR_TIMEOUT"}
+          -5: "QGEMM_ERR_CUDA", -6: "QGEMM_ERR_TIMEOUT", -7: "QGEMM_ERR_IO"}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemm.so")
 _lib = None
@@ -47,6 +47,9 @@ SIGNATURES = {
     "qgemm_w4a8_acc_workspace_bytes": ([_I, _I], _SZ),
     "qgemm_status": ([_P], _I),
     "qgemm_run_noalloc": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P], _I),
+    "qgemm_save": ([ctypes.c_char_p, _I, _I, _I, _I, _I, _P, _P, _I, _P], _I),
+    "qgemm_load_info": ([ctypes.c_char_p] + [ctypes.POINTER(ctypes.c_int)] * 5, _I),
+    "qgemm_load": ([ctypes.c_char_p, _P, _SZ, _P, _SZ, _I, _P], _I),
     "qgemm_set_option": ([_I, _I], _I),
     "qgemm_get_option": ([_I], _I),
     "qgemm_error_string": ([_I], ctypes.c_char_p),
@@ -82,7 +85,18 @@ def _ptr(x):
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data      # a numpy array (host memory)
+
+
+def _on_device(*xs) -> int:
+    """1 if the given buffers (torch tensors or numpy arrays; None ignored) are on the GPU, 0 if
+    on the host; mixed placements are an error."""
+    where = {bool(getattr(x, "is_cuda", False)) for x in xs if x is not None}
+    if len(where) > 1:
+        raise ValueError("Bp and T must both be device tensors or both host buffers")
+    return int(where.pop()) if where else 0
 
 
 def _stream(stream):
@@ -115,6 +129,28 @@ def qgemm_workspace_bytes(M: int, K: int, N: int, mode: int, block: int, a_dtype
 # ---------------------------------------------------------------- compute
 def qgemm_pack(W, K: int, N: int, mode: int, block: int, w_dtype: int, Bp, T, stream=None) -> None:
     _check(load().qgemm_pack(_ptr(W), K, N, mode, block, w_dtype, _ptr(Bp), _ptr(T), _stream(stream)), "qgemm_pack")
+
+
+def qgemm_save(path: str, K: int, N: int, mode: int, block: int, w_dtype: int, Bp, T, stream=None) -> None:
+    """Writes a packed layer (qgemm_pack's Bp and T, device tensors or host buffers) to `path`."""
+    dev = _on_device(Bp, T)
+    _check(load().qgemm_save(os.fsencode(path), K, N, mode, block, w_dtype, _ptr(Bp), _ptr(T), dev,
+                             _stream(stream) if dev else None), "qgemm_save")
+
+
+def qgemm_load_info(path: str) -> dict:
+    """The shape and format of a packed-weight file: {K, N, mode, block, w_dtype}."""
+    vals = [ctypes.c_int() for _ in range(5)]
+    _check(load().qgemm_load_info(os.fsencode(path), *[ctypes.byref(v) for v in vals]), "qgemm_load_info")
+    return dict(zip(("K", "N", "mode", "block", "w_dtype"), (v.value for v in vals)))
+
+
+def qgemm_load(path: str, Bp, T, stream=None) -> None:
+    """Reads a packed-weight file into Bp and T (device tensors or host buffers, large enough)."""
+    nbytes = lambda x: 0 if x is None else (x.numel() * x.element_size() if hasattr(x, "numel") else x.nbytes)
+    dev = _on_device(Bp, T)
+    _check(load().qgemm_load(os.fsencode(path), _ptr(Bp), nbytes(Bp), _ptr(T), nbytes(T), dev,
+                             _stream(stream) if dev else None), "qgemm_load")
 
 
 def qgemm_run(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, C, c_dtype: int,

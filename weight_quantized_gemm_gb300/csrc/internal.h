@@ -107,6 +107,10 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
 
 // library options (qgemm_set_option)
 int option_overlap();
+// Records `detail` as the thread's last error and returns `code` (the C ABI's error path).
+int api_fail(int code, const char* detail);
+// Bp bytes of a shape (0 if the shape is invalid) and, in *table_bytes, its T bytes (0 in FLOAT).
+size_t api_packed_bytes(int K, int N, int mode, int block, int w_dtype, size_t* table_bytes);
 
 // device status word (bounded waits that gave up); read and cleared by qgemm_status
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);

@@ -105,6 +105,15 @@ size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool requir
 
 int qg::option_overlap() { return g_opt_overlap.load(std::memory_order_relaxed); }
 
+int qg::api_fail(int code, const char* detail) { return fail(code, "%s", detail); }
+size_t qg::api_packed_bytes(int K, int N, int mode, int block, int w_dtype, size_t* table_bytes) {
+    *table_bytes = 0;
+    if (check_shape(K, N, mode, &block) != QGEMM_OK) return 0;
+    if (mode == QGEMM_MODE_FLOAT && !valid_dtype(w_dtype)) return 0;
+    if (mode != QGEMM_MODE_FLOAT) *table_bytes = qg::table_pairs(N, K / block) * 2 * sizeof(float);
+    return packed_bytes(K, N, mode, w_dtype);
+}
+
 extern "C" {
 
 int qgemm_set_option(int option, int value) {
@@ -352,6 +361,7 @@ const char* qgemm_error_string(int code) {
         case QGEMM_ERR_WORKSPACE: return "QGEMM_ERR_WORKSPACE";
         case QGEMM_ERR_CUDA: return "QGEMM_ERR_CUDA";
         case QGEMM_ERR_TIMEOUT: return "QGEMM_ERR_TIMEOUT";
+        case QGEMM_ERR_IO: return "QGEMM_ERR_IO";
         default: return "QGEMM_ERR_UNKNOWN";
     }
 }
