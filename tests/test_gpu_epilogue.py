@@ -84,3 +84,16 @@ def test_fused_epilogue_parts(M, K, N, mode, block, a_dtype, c_dtype):
 def test_fused_epilogue_f32_output_of_16bit_path():
     fused_case(33, 1024, 200, 1, 64, synth.F16, synth.F32, qg.ACT_GELU_TANH, True, "separate")
 
+
+
+def test_fused_epilogue_residual_after_long_k():
+    """Tensor cores without K-splits over many stages: the residual tile's TMA load into the
+    staging area must wait for the last use of every ring slot it overwrites (int4 on 256-row
+    tiles, and W4A8 on 128-row tiles with two sub-stages per stage)."""
+    prev = qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
+    try:
+        fused_case(200, 4096, 384, 1, 64, synth.F16, synth.BF16, qg.ACT_SILU, True, "separate")
+        fused_case(200, 4096, 384, 1, 64, synth.F16, synth.BF16, qg.ACT_NONE, False, "inplace")
+        fused_case(100, 2048, 256, 3, 0, synth.BF16, synth.BF16, qg.ACT_GELU_TANH, True, "inplace")
+    finally:
+        qg.qgemm_set_option(qg.OPT_SPLIT_K, prev)

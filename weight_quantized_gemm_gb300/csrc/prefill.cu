@@ -62,6 +62,7 @@ struct Params {
     const int32_t* rowsum;    // W4A8: per-row sum of activation codes
     int32_t* acc;             // EPI_ACC output
     int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
+    int r_tma;                // the epilogue's residual tile comes in by one TMA load (Maps::r)
     int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
     int tblocks;              // K-blocks per table box (min(SUB, nb))
     Epilogue ep;              // bias / activation / residual (none when the output is split partials)
@@ -268,6 +269,15 @@ __device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float 
 }
 
 template <int CDT>
+__device__ __forceinline__ float load_s(const void* C, size_t idx) {   // element of a staged tile
+    if constexpr (CDT == DT_F32)
+        return static_cast<const float*>(C)[idx];
+    else if constexpr (CDT == DT_F16)
+        return __half2float(static_cast<const __half*>(C)[idx]);
+    else
+        return __bfloat162float(static_cast<const __nv_bfloat16*>(C)[idx]);
+}
+template <int CDT>
 __device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
     if constexpr (CDT == DT_F32)
         static_cast<float*>(C)[idx] = v;
@@ -331,6 +341,7 @@ struct Maps {                 // the kernel's tensor maps
     CUtensorMap w;            // packed weights
     CUtensorMap t;            // grouped {offset, scale} table (formats with a table)
     CUtensorMap c;            // the output, when Params::c_tma (stored by TMA from the staged tile)
+    CUtensorMap r;            // the epilogue's residual, when Params::r_tma (same layout as c)
 };
 
 // One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), and the
@@ -359,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
     // bars: full[S] (the stage's boxes landed) | full_a[S] (TMEM A stage written) |
     //       empty[S] (MMAs of the stage done) | acc_full
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 1);
+    // ... | res_full (the residual tile landed, Params::r_tma)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
     float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
@@ -368,6 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto full_a = [&](int s) { return smem_u32(bars + kMaxStages + s); };
     auto empty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + s); };
     const uint32_t acc_full = smem_u32(bars + 3 * kMaxStages);
+    const uint32_t res_full = smem_u32(bars + 3 * kMaxStages + 1);
+    // bytes of the staged output tile [BN rows][128 channels], where the residual tile also lands
+    constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
+    static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -376,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(empty(s), 1);    // one tcgen05.commit per use
         }
         mbar_init(acc_full, 1);
+        mbar_init(res_full, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
@@ -419,6 +436,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
                     volatile int never = 0;
                     mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never);
+                }
+            } else if (EPI != EPI_ACC && p.r_tma) {
+                // The residual tile lands where the output tile is staged, [0, kTileBytes): as
+                // soon as the MMAs of the last use of every ring slot under that range are done
+                // (a few stages before the end of K), one TMA load brings it in, so its latency
+                // hides behind the last stages.
+                bool free = true;
+                for (int sl = 0; sl < S && (uint32_t)sl * SB < kTileBytes && free; ++sl) {
+                    if (sl >= nks) break;                              // never used
+                    const int last = sl + ((nks - 1 - sl) / S) * S;    // its last use
+                    free = mbar_wait(empty(sl), (uint32_t)(last / S) & 1u, abort_flag);
+                }
+                if (free) {
+                    mbar_expect_tx(res_full, kTileBytes);
+                    ptx::tma_load_3d(st_s, &maps.r, n_tile, m_tile, 0, res_full);
+                    volatile int never = 0;   // stay until it has landed (the epilogue reads it)
+                    mbar_wait(res_full, 0u, &never);
                 }
             }
         }
@@ -535,12 +569,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             // warp each) before any of them is used; the activation is chosen once per chunk.
             const bool has_ep = EPI != EPI_ACC && p.ep.any();
             const bool has_res = has_ep && p.ep.residual != nullptr;
+            // the residual tile, when it came in by TMA, sits where this thread stages its outputs:
+            // each element is read and then overwritten by the same thread
+            const bool res_smem = has_res && p.r_tma && mbar_wait(res_full, 0u, abort_flag);
+            const bool res_glob = has_res && !p.r_tma;
             const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
             for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kAccCol + c0, v);
                 float rv[32];
-                if (has_res) {
+                if (res_glob) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int m = m_tile + c0 + i;
@@ -582,9 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                 break;
                             default: break;
                         }
-                        if (has_res) {
+                        if (res_glob) {
 #pragma unroll
                             for (int i = 0; i < 32; ++i) y[i] += rv[i];
+                        } else if (res_smem) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) y[i] += load_s<CDT>(tile, (size_t)(c0 + i) * kBM + r);
                         }
                     }
 #pragma unroll
@@ -850,6 +891,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     p.c_tma = pf::make_out_map(&maps.c, p.C, kdt, a.M, a.N, p.BN, p.splits) ? 1 : 0;
     if (!p.c_tma) maps.c = maps.a;             // unused
+    p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), kdt, a.M, a.N, p.BN, 1) ? 1 : 0;
+    if (!p.r_tma) maps.r = maps.a;             // unused
     if (a.fmt == FMT_INT4)
         e = bf ? pf::launch_wf<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, kdt, s)
                : pf::launch_wf<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, kdt, s);
@@ -876,6 +919,9 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN, 1) ? 1 : 0)
                     : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN, 1) ? 1 : 0);
     if (!p.c_tma) maps.c = maps.a;     // unused
+    p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), a.c_dtype, a.M, a.N, p.BN, 1)
+                  ? 1 : 0;
+    if (!p.r_tma) maps.r = maps.a;     // unused
     if (a.acc) return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_ACC>(maps, p, DT_F32, s);
     return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
 }
