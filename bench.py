@@ -88,16 +88,18 @@ def src_hash(kernel: str) -> str:
 
 def measured_traffic(w: synth.Workload):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    (profiles/traffic.txt: workload kernel source-hash bytes), if it was taken on this source."""
+    (profiles/traffic.txt: workload M K N kernel source-hash bytes), if it was taken on this
+    shape and this source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     kern = kernel_of(w)
     cur = src_hash(kern)
+    key = [w.name, str(w.M), str(w.K), str(w.N), kern, cur]
     for ln in open(path):
         parts = ln.split()
-        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == w.name and parts[1] == kern and parts[2] == cur:
-            return int(float(parts[3]))
+        if len(parts) >= 7 and not ln.startswith("#") and parts[:6] == key:
+            return int(float(parts[6]))
     return None
 
 
