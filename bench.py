@@ -68,8 +68,8 @@ def bound_of(w: synth.Workload) -> str:
 # while these files are unchanged since the capture
 KERNEL_SOURCES = {
     "decode": ["decode_stream.cuh", "decode_kernel.cuh", "decode_int4.cu", "decode_int8.cu", "decode_float.cu",
-               "ptx.cuh", "internal.h"],
-    "prefill": ["prefill.cu", "ptx.cuh", "internal.h"],
+               "epilogue.cuh", "ptx.cuh", "internal.h"],
+    "prefill": ["prefill_kernel.cuh", "prefill.cu", "prefill_codes.cu", "epilogue.cuh", "ptx.cuh", "internal.h"],
 }
 
 
@@ -418,6 +418,8 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--k", type=int, default=0, help="override the workload's K (e.g. the MNN shape grid)")
     ap.add_argument("--n", type=int, default=0, help="override the workload's N (e.g. the MNN shape grid)")
+    ap.add_argument("--a-dtype", default="", choices=["", "f16", "bf16", "f32"],
+                    help="override the workload's activation dtype")
     ap.add_argument("--decode-max-m", type=int, default=0,
                     help="QGEMM_OPT_DECODE_MAX_M for the run (the decode / tensor-core crossover)")
     ap.add_argument("--no-split-k", action="store_true",
@@ -435,9 +437,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    import dataclasses
     w = synth.WORKLOADS[args.workload]
+    if args.a_dtype:
+        w = dataclasses.replace(w, a_dtype={"f16": synth.F16, "bf16": synth.BF16, "f32": synth.F32}[args.a_dtype])
     if args.m or args.k or args.n:
-        import dataclasses
         w = dataclasses.replace(w, M=args.m or w.M, K=args.k or w.K, N=args.n or w.N)
 
     if args.print_src_hash:

@@ -87,7 +87,10 @@ size_t qgemm_table_bytes(int K, int N, int mode, int block);
 /* Bytes of scratch device memory qgemm_run uses for this call (0 if none). The decode path
  * needs it when it splits K across thread blocks (small N); W4A8 needs it for the quantized
  * activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums). The tensor-core
- * path (M above QGEMM_OPT_DECODE_MAX_M) uses it for float32 partial sums when it splits K
+ * path (M above QGEMM_OPT_DECODE_MAX_M) needs 4*M bytes (256-byte aligned) for the row sums of A
+ * in INT8 mode with block = K, bf16 activations and M >= 256 (the per-channel scale and offset are
+ * then applied in its epilogue), and
+ * uses the rest for float32 partial sums when it splits K
  * (mid-sized M, few 128-channel tiles): splits*M*N*4 bytes. That part is optional: qgemm_run
  * given less scratch splits K fewer times (down to none), which changes only the float32
  * summation order of the result. */

@@ -44,9 +44,12 @@ def test_prefill_output_dtypes(c_dtype):
     (96, 1600, 1000, 2, 0, synth.BF16, 3),     # uneven splits (8, 8, 9), per-channel int8
     (48, 2048, 384, 1, 128, synth.BF16, 4),    # bf16 hi/lo weight parts, K-blocks across splits
     (33, 1024, 256, 0, 0, synth.BF16, 2),      # float mode
+    (256, 2048, 256, 2, 0, synth.BF16, 4),     # Int8-Block0 codes path: the offset term in split 0 only
 ])
 def test_prefill_split_k(M, K, N, mode, block, a_dtype, splits):
-    assert qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, a_dtype) == splits * M * N * 4
+    # Int8-Block0 row sums (the codes path: bf16, M >= 256)
+    rows = -(-M * 4 // 256) * 256 if (mode == 2 and block == 0 and a_dtype == synth.BF16 and M >= 256) else 0
+    assert qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, a_dtype) == rows + splits * M * N * 4
     layer_case(M, K, N, mode, block, a_dtype, a_dtype)
 
 

@@ -147,7 +147,37 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
     }
 }
 
+// Row sums of A in float32 (the Int8-Block0 tensor-core path's offset term o * sum_k a): one
+// warp per row, 8 consecutive values per lane and step (16-byte loads), a shuffle reduction.
+template <int ADT>
+__global__ void __launch_bounds__(kThreads) row_sum_kernel(int M, int K, const void* __restrict__ A,
+                                                           float* __restrict__ out) {
+    const int m = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (m >= M) return;
+    float acc = 0.f;
+    for (int k = lane * 8; k < K; k += 32 * 8) {
+        float v[8];
+        load8<ADT>(A, (size_t)m * K + k, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) out[m] = acc;
+}
+
 }  // namespace
+
+cudaError_t launch_row_sums(int M, int K, const void* A, int a_dtype, float* out, cudaStream_t s) {
+    const int blocks = (M + kThreads / 32 - 1) / (kThreads / 32);
+    if (a_dtype == DT_F32)
+        row_sum_kernel<DT_F32><<<blocks, kThreads, 0, s>>>(M, K, A, out);
+    else if (a_dtype == DT_F16)
+        row_sum_kernel<DT_F16><<<blocks, kThreads, 0, s>>>(M, K, A, out);
+    else
+        row_sum_kernel<DT_BF16><<<blocks, kThreads, 0, s>>>(M, K, A, out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
                              int32_t* rowsum, cudaStream_t s) {

@@ -79,7 +79,16 @@ struct PrefillArgs {
     float* partial;   // [splits][M][N] f32 partial sums when splits > 1
     int splits;       // K-splits across thread blocks (>= 1), from prefill_splits
     Epilogue ep;
+    float* rowsum;    // [M] scratch for the row sums of A (Int8-Block0 on the codes path)
 };
+// Int8-Block0 (per-channel) layers with bf16 activations and M >= 256 run on the tensor cores as
+// raw codes with the scale and offset applied in the epilogue (they need [M] float32 row sums of A
+// as scratch): the codes are exact in bf16, so the hi/lo weight split and its second MMA go away
+// (measured at M = 1024: 33 us against 44). With f16 activations, or fewer rows, the row-sum
+// pre-pass costs more than it saves and the dequantizing path stays.
+inline bool prefill_codes_path(int fmt, int K, int block, int M, int a_dtype) {
+    return fmt == FMT_INT8 && block == K && a_dtype == DT_BF16 && M >= 256;
+}
 // K-splits the tensor-core kernel uses for this shape (1 = none); host-only, no GPU needed.
 int prefill_splits(int M, int K, int N, int fmt);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
@@ -90,6 +99,8 @@ bool prefill_supported(int M, int K, int N, int fmt, int a_dtype);
 cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
                              int32_t* rowsum, cudaStream_t s);
 cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s);
+// out[m] = sum_k A[m][k] in float32 (the Int8-Block0 tensor-core path's row sums)
+cudaError_t launch_row_sums(int M, int K, const void* A, int a_dtype, float* out, cudaStream_t s);
 // acc (int32 [M][N]) = qa x q^T; or, when acc == nullptr, the rescaled output into C.
 struct W4A8Args {
     int M, K, N;

@@ -1,813 +1,13 @@
-// Tensor-core path for larger M (prefill) and for W4A8: tcgen05 MMA with TMEM accumulators.
-//
-// The layer C[M,N] = A[M,K] x dequant(B[K,N]) (benchmark page "MNN GemmSpeed 基准测试实战",
-// «为什么用 Conv1x1 来测 GEMM») is computed transposed, D[n][m] = sum_k W[n][k] * A[m][k], so that
-// the operand that needs work before it can be multiplied -- the packed weight -- is the MMA's
-// A operand and lives in tensor memory, while the activations stream in by TMA:
-//   - a TMA warp loads, per pipeline stage, the stage's K slice of A (up to 256 rows, 128-byte
-//     swizzle), the packed weight rows of the 128-channel tile and their {offset, scale} table
-//     entries into shared memory; a stage is one or two 64-wide sub-stages of K;
-//   - dequant warps rebuild w = q * scale + offset in float32 (one rounding to the activation's
-//     16-bit type) and write them into a TMEM stage with tcgen05.st;
-//   - one thread issues tcgen05.mma (kind::f16, M = 128, N = tile rows of A, K = 16 per
-//     instruction) with A from TMEM and B from shared memory, accumulating in TMEM, and
-//     commits each stage back to the producers;
-//   - after the last stage the dequant warps read the accumulator with tcgen05.ld, stage the
-//     tile in shared memory and store it (one TMA store where the rows allow).
-// Shapes whose tiles fill less than one wave of SMs split K across blocks (grid z): each split
-// writes float32 partial sums and a second kernel adds them in a fixed order.
-// W4A8 ("W4 解包为 INT8 ... S8×S8→S32", «测试用例与注册机制») uses the same kernel with the 4-bit
-// codes as exact f16 integers and the activation codes as exact f16 integers: every product is
-// an integer below 2^11 and every partial sum an integer below 2^24, so the float32 tensor-core
-// accumulation is exact and equals the int32 sum; the epilogue then either stores it as int32
-// or applies as * (ws * acc + off * rowsum).
-//
-// Every wait on an mbarrier is bounded: a wait that runs out sets the library's status word and
-// an abort flag, all roles leave their loops, in-flight work is drained (bounded) and TMEM is
-// freed before the kernel returns.
-#include <cuda.h>
+// Tensor-core path, dequantizing forms (Int4 / Int8 per K-block, float mode) and the shared
+// host logic: K-split choice, the library's device status word, the tensor-map encoder.
 #include <mutex>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 
-#include "epilogue.cuh"
-#include "internal.h"
-#include "ptx.cuh"
+#include "prefill_kernel.cuh"
 
 namespace qg {
 
 // Set (bitwise OR) by a kernel that gave up a bounded wait; read and cleared by qgemm_status.
 __device__ unsigned int g_status_word;
-
-namespace pf {
-
-constexpr int kBM = 128;              // output channels per tile (MMA M)
-constexpr int kBK = 64;               // K per pipeline stage
-constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
-constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
-constexpr int kThreads = kWarps * 32;
-constexpr int kEpiThreads = (kWarps - 2) * 32;   // dequant + epilogue threads
-constexpr int kTmemCols = 512;
-constexpr int kAccCol = 0;            // accumulator columns [0, BN); the A stages follow
-
-enum Wf { WF_INT4 = 0, WF_INT8 = 1, WF_FLOAT = 2, WF_CODES4 = 3 };
-enum Epi { EPI_STORE = 0, EPI_W4A8 = 1, EPI_ACC = 2 };
-
-struct Params {
-    int M, K, N, block, nb, BN;
-    const uint8_t* Bp;
-    const float* T;
-    void* C;
-    const float* a_scale;     // W4A8: per-row activation scale
-    const int32_t* rowsum;    // W4A8: per-row sum of activation codes
-    int32_t* acc;             // EPI_ACC output
-    int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
-    int r_tma;                // the epilogue's residual tile comes in by one TMA load (Maps::r)
-    int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
-    int tblocks;              // K-blocks per table box (min(SUB, nb))
-    Epilogue ep;              // bias / activation / residual (none when the output is split partials)
-};
-
-// ---------------------------------------------------------------- PTX helpers
-using ptx::mbar_arrive;
-using ptx::mbar_expect_tx;
-using ptx::mbar_init;
-using ptx::smem_u32;
-using ptx::tma_load_2d;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    return ptx::mbar_wait(bar, parity, abort_flag, &g_status_word);
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// D (TMEM) (+)= A (TMEM) x B (shared memory, descriptor)
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
-            d),
-        "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D (TMEM) (+)= A (shared memory, descriptor) x B (shared memory, descriptor)
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-            d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ uint4 lds128u(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ float2 lds64f(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
-          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-          "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte swizzle: rows of
-// 128 bytes (64 16-bit elements), 8-row swizzle atoms 1024 bytes apart (stride byte offset),
-// descriptor version 1, swizzle mode 2 (128 B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: D float32, A and B both f16 (0) or both bf16 (1), both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t idesc_f16(bool bf16, int n, int m) {
-    const uint32_t ab = bf16 ? 1u : 0u;
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
-    uint32_t d;
-    if (bf16)
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    else
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-
-// Dequantized weights with bf16 activations are split as w = hi + lo with hi = bf16(w) and
-// lo = bf16(w - hi): the MMA then multiplies both parts, which keeps the weight to about 2^-17
-// relative instead of bf16's 2^-9 (f16 weights are kept to 2^-12 by one rounding).
-template <int WF, bool BF>
-struct Split {
-    static constexpr bool kOn = BF && (WF == WF_INT4 || WF == WF_INT8);
-    static constexpr int kStageCols = kOn ? 64 : 32;
-};
-
-__device__ __forceinline__ uint32_t pack2_split(float lo, float hi, uint32_t& rest) {
-    const uint32_t h = pack2(lo, hi, true);
-    const float l0 = lo - __uint_as_float(h << 16), l1 = hi - __uint_as_float(h & 0xFFFF0000u);
-    rest = pack2(l0, l1, true);
-    return h;
-}
-
-// Exact float32 values of 4- and 8-bit codes without an integer conversion: a code placed in
-// mantissa bits 15..18 of the float 256.0 reads 256 + q, in bits 19..22 of 16.0 it reads 16 + q,
-// and an 8-bit code in bits 15..22 of 256.0 reads 256 + q. The bias folds into the offset, so
-// w = q * s + o = fma(bias + q, s, o - bias * s) is a single rounding of the exact value plus the
-// rounding of o - bias * s (at most 2^-24 * (|o| + 256 s), which is negligible).
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
-    return d;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-// (x0, x1) * (s, s) + (c0, c1) in one packed float32 instruction
-__device__ __forceinline__ void fma2(float x0, float x1, float s, float c0, float c1, float& r0, float& r1) {
-    asm("{\n\t.reg .b64 x, y, z, d;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %4};\n\tmov.b64 z, {%5, %6};\n\t"
-        "fma.rn.f32x2 d, x, y, z;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(r0), "=f"(r1)
-        : "f"(x0), "f"(x1), "f"(s), "f"(c0), "f"(c1));
-}
-// byte j of w moved to bits 15..22
-template <int J>
-__device__ __forceinline__ uint32_t byte_to_15(uint32_t w) {
-    if constexpr (8 * J < 15) return w << (15 - 8 * J);
-    else return w >> (8 * J - 15);
-}
-
-// The 32 weights (k = k0 .. k0 + 31 of one channel row) this thread converts for one stage,
-// as 16 packed 16-bit pairs (low half = even k); with Split, rest gets the low parts. raw holds
-// the packed bytes.
-template <int WF, bool BF>
-__device__ __forceinline__ void convert32(const uint4 (&raw)[4], float s, float o, uint32_t (&out)[16],
-                                          uint32_t (&rest)[16]) {
-    constexpr bool kSplit = Split<WF, BF>::kOn;
-    auto emit = [&](int idx, float w0, float w1) {
-        if constexpr (kSplit) out[idx] = pack2_split(w0, w1, rest[idx]);
-        else out[idx] = pack2(w0, w1, BF);
-    };
-    if constexpr (WF == WF_INT4) {
-        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};   // 32 nibbles, byte j = (k 2j, 2j+1)
-        const float c_lo = fmaf(-256.f, s, o), c_hi = fmaf(-16.f, s, o);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t t[4] = {byte_to_15<0>(w[i]), byte_to_15<1>(w[i]), byte_to_15<2>(w[i]), byte_to_15<3>(w[i])};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float q0 = __uint_as_float(lop3_and_or(t[j], 0x00078000u, 0x43800000u));   // 256 + low nibble
-                const float q1 = __uint_as_float(lop3_and_or(t[j], 0x00780000u, 0x41800000u));   // 16 + high nibble
-                float w0, w1;
-                fma2(q0, q1, s, c_lo, c_hi, w0, w1);
-                emit(4 * i + j, w0, w1);
-            }
-        }
-    } else if constexpr (WF == WF_CODES4) {
-        // the codes themselves, exact in f16: (1024 + lo, 1024 + 16 hi) -> (lo, hi)
-        const uint32_t w[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t v = lop3_and_or(prmt(w[i], w[i], 0x4040u + 0x0101u * j), 0x00F0000Fu, 0x64006400u);
-                uint32_t d;
-                asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(v), "r"(0x2C003C00u), "r"(0xD400E400u));
-                out[4 * i + j] = d;
-            }
-        }
-    } else if constexpr (WF == WF_INT8) {
-        const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
-        const float c8 = fmaf(-256.f, s, o);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float q0 = __uint_as_float(lop3_and_or(byte_to_15<0>(w[i]), 0x007F8000u, 0x43800000u));
-            const float q1 = __uint_as_float(lop3_and_or(byte_to_15<1>(w[i]), 0x007F8000u, 0x43800000u));
-            const float q2 = __uint_as_float(lop3_and_or(byte_to_15<2>(w[i]), 0x007F8000u, 0x43800000u));
-            const float q3 = __uint_as_float(lop3_and_or(byte_to_15<3>(w[i]), 0x007F8000u, 0x43800000u));
-            float w0, w1, w2, w3;
-            fma2(q0, q1, s, c8, c8, w0, w1);
-            fma2(q2, q3, s, c8, c8, w2, w3);
-            emit(2 * i, w0, w1);
-            emit(2 * i + 1, w2, w3);
-        }
-    } else {
-        const uint32_t w[16] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w,
-                                raw[2].x, raw[2].y, raw[2].z, raw[2].w, raw[3].x, raw[3].y, raw[3].z, raw[3].w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) out[i] = w[i];
-    }
-}
-
-template <int CDT>
-__device__ __forceinline__ float load_s(const void* C, size_t idx) {   // element of a staged tile
-    if constexpr (CDT == DT_F32)
-        return static_cast<const float*>(C)[idx];
-    else if constexpr (CDT == DT_F16)
-        return __half2float(static_cast<const __half*>(C)[idx]);
-    else
-        return __bfloat162float(static_cast<const __nv_bfloat16*>(C)[idx]);
-}
-template <int CDT>
-__device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
-    if constexpr (CDT == DT_F32)
-        static_cast<float*>(C)[idx] = v;
-    else if constexpr (CDT == DT_F16)
-        static_cast<__half*>(C)[idx] = __float2half_rn(v);
-    else
-        static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
-}
-
-// Shared-memory stage of SUB sub-stages (SUB x 64 of K), at a multiple of 1024 bytes:
-//   [SUB activation boxes, each [BN rows][128 B] with the 128-byte swizzle]
-//   [weights: one box [128 rows][SUB x row bytes of a sub-stage] for the quantized formats, or
-//    (float mode, SUB = 1) the 16-bit weights [128 rows][128 B] with the 128-byte swizzle, read by
-//    the MMA directly as its A operand]
-//   [formats with a table: the {offset, scale} entries of the stage's (up to) SUB K-blocks for the
-//    tile's 128 channels, [8 groups of 16][SUB x 32 floats] in the grouped table layout]
-// One stage is one round of the pipeline's barriers, so SUB = 2 halves the waits, arrivals and
-// commits per unit of K; the ring holds as many stages as shared and tensor memory allow.
-constexpr size_t kSmemMax = 232448;                 // opt-in shared memory per block
-constexpr int kTail = 256 + kMaxBN * 8;              // barriers + W4A8 row factors after the ring
-constexpr int kRing = (int)kSmemMax - kTail;         // bytes for the stages
-constexpr int kMaxStages = 8;
-template <int WF>
-struct WBox {   // bytes of one channel row of one 64-wide sub-stage
-    static constexpr int kRowBytes = (WF == WF_INT4 || WF == WF_CODES4) ? kBK / 2 : (WF == WF_INT8 ? kBK : 2 * kBK);
-};
-template <int WF, bool BF, int SUB>
-struct Geo {
-    static constexpr bool kTable = WF == WF_INT4 || WF == WF_INT8;
-    static constexpr int kWBytes = kBM * SUB * WBox<WF>::kRowBytes;
-    static constexpr int kTBytes = kTable ? SUB * (kBM / 16) * 128 : 0;
-    static constexpr int kCols = SUB * Split<WF, BF>::kStageCols;   // TMEM columns of one A stage
-    static constexpr int stage_bytes(int BN) { return SUB * BN * kBK * 2 + kWBytes + kTBytes; }
-    // stages in the ring for tile height BN: what shared memory holds, and what tensor memory
-    // holds beside the BN accumulator columns
-    static constexpr int stages(int BN) {
-        return kRing / stage_bytes(BN) < (kTmemCols - BN) / kCols
-                   ? (kRing / stage_bytes(BN) < kMaxStages ? kRing / stage_bytes(BN) : kMaxStages)
-                   : ((kTmemCols - BN) / kCols < kMaxStages ? (kTmemCols - BN) / kCols : kMaxStages);
-    }
-};
-// The kernel's shape for tile height BN, fixed at compile time: two 64-wide sub-stages per stage
-// (half the barrier rounds per unit of K) where the ring still holds at least kMinSub2Stages of
-// them -- small tiles, whose stages are short and whose per-round costs dominate; large tiles keep
-// 64-wide stages, whose finer-grained ring refills sooner.
-constexpr int kMinSub2Stages = 5;
-template <int WF, bool BF, int BN>
-struct Plan {
-    static constexpr int kSub = (WF != WF_FLOAT && Geo<WF, BF, 2>::stages(BN) >= kMinSub2Stages) ? 2 : 1;
-    using G = Geo<WF, BF, kSub>;
-    static constexpr int kStages = G::stages(BN);
-    static constexpr int kStageBytes = G::stage_bytes(BN);
-    static_assert(WF != WF_FLOAT || kSub == 1, "float mode loads one swizzled weight box per stage");
-    static_assert(kStages >= 2 && kStages <= kMaxStages, "ring of at least two stages");
-    static_assert(kStages * kStageBytes <= kRing, "ring fits in shared memory");
-    static_assert(BN + kStages * G::kCols <= kTmemCols, "accumulator and A stages fit in TMEM");
-    static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle atoms)");
-};
-struct Maps {                 // the kernel's tensor maps
-    CUtensorMap a;            // activations
-    CUtensorMap w;            // packed weights
-    CUtensorMap t;            // grouped {offset, scale} table (formats with a table)
-    CUtensorMap c;            // the output, when Params::c_tma (stored by TMA from the staged tile)
-    CUtensorMap r;            // the epilogue's residual, when Params::r_tma (same layout as c)
-};
-
-// One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), and the
-// stages of K-split z (all of K when p.splits == 1).
-template <int WF, bool BF, int EPI, int CDT, int BN>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Maps maps, Params p) {
-    using P = Plan<WF, BF, BN>;
-    using G = typename P::G;
-    constexpr int SUB = P::kSub, S = P::kStages;
-    constexpr uint32_t SB = P::kStageBytes;
-    constexpr bool kDequant = WF != WF_FLOAT;          // weights go through the dequant warps into TMEM
-    constexpr int kRowB = WBox<WF>::kRowBytes;
-    constexpr int kLo = SUB * 32;                      // TMEM column of the low parts in an A stage (Split)
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr uint32_t kABytes = (uint32_t)BN * kBK * 2;   // one activation box
-    constexpr uint32_t w_off = SUB * kABytes, t_off = w_off + G::kWBytes;
-    const int n_tile = blockIdx.x * kBM, m_tile = blockIdx.y * BN;
-    const int nsub = p.K / kBK;                        // 64-wide sub-stages of K
-    const int nst = (nsub + SUB - 1) / SUB;            // stages (the last may be half past K: reads 0)
-    // split z covers stages [ks0, ks0 + nks); the ring counts stages from 0 within the split
-    const int ks0 = (int)((long long)nst * blockIdx.z / p.splits);
-    const int nks = (int)((long long)nst * (blockIdx.z + 1) / p.splits) - ks0;
-    const int bpb = p.block / kBK;                     // sub-stages per table block
-
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
-    // bars: full[S] (the stage's boxes landed) | full_a[S] (TMEM A stage written) |
-    //       empty[S] (MMAs of the stage done) | acc_full
-    // ... | res_full (the residual tile landed, Params::r_tma)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
-    float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
-    const uint32_t st_s = smem_u32(smem);
-    auto full_x = [&](int s) { return smem_u32(bars + s); };
-    auto full_a = [&](int s) { return smem_u32(bars + kMaxStages + s); };
-    auto empty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + s); };
-    const uint32_t acc_full = smem_u32(bars + 3 * kMaxStages);
-    const uint32_t res_full = smem_u32(bars + 3 * kMaxStages + 1);
-    // bytes of the staged output tile [BN rows][128 channels], where the residual tile also lands
-    constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
-    static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(full_x(s), 1);
-            mbar_init(full_a(s), 8);   // one arrival per dequant warp
-            mbar_init(empty(s), 1);    // one tcgen05.commit per use
-        }
-        mbar_init(acc_full, 1);
-        mbar_init(res_full, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        ptx::prefetch_tmap(&maps.a);
-        ptx::prefetch_tmap(&maps.w);
-        if constexpr (G::kTable) ptx::prefetch_tmap(&maps.t);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t a_col = tmem + (uint32_t)BN;        // A stages follow the BN accumulator columns
-
-    if (warp == 0) {
-        // ---------------- TMA producer: per stage the SUB activation boxes, the weight box and
-        // (formats with a table) the {offset, scale} entries of the stage's K-blocks
-        if (lane == 0) {
-            const uint32_t bytes = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
-            int issued = 0, s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; i < nks; ++i) {
-                const int ks = ks0 + i;
-                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                mbar_expect_tx(full_x(s), bytes);
-#pragma unroll
-                for (int j = 0; j < SUB; ++j)
-                    tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
-                // weight box: x in bytes for the packed formats, in elements for float mode
-                tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
-                if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
-                                           // (the box holds tblocks K-blocks, the stage's first one first)
-                    tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
-                issued = i + 1;
-                if (++s == S) { s = 0; ph ^= 1u; }
-            }
-            if (*abort_flag) {   // let the copies already issued land before the block exits
-                for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
-                    volatile int never = 0;
-                    mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never);
-                }
-            } else if (EPI != EPI_ACC && p.r_tma) {
-                // The residual tile lands where the output tile is staged, [0, kTileBytes): as
-                // soon as the MMAs of the last use of every ring slot under that range are done
-                // (a few stages before the end of K), one TMA load brings it in, so its latency
-                // hides behind the last stages.
-                bool free = true;
-                for (int sl = 0; sl < S && (uint32_t)sl * SB < kTileBytes && free; ++sl) {
-                    if (sl >= nks) break;                              // never used
-                    const int last = sl + ((nks - 1 - sl) / S) * S;    // its last use
-                    free = mbar_wait(empty(sl), (uint32_t)(last / S) & 1u, abort_flag);
-                }
-                if (free) {
-                    mbar_expect_tx(res_full, kTileBytes);
-                    ptx::tma_load_3d(st_s, &maps.r, n_tile, m_tile, 0, res_full);
-                    volatile int never = 0;   // stay until it has landed (the epilogue reads it)
-                    mbar_wait(res_full, 0u, &never);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16(BF, BN, kBM);
-            int s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; i < nks; ++i) {
-                if constexpr (kDequant)
-                    if (!mbar_wait(full_a(s), ph, abort_flag)) break;
-                if (!mbar_wait(full_x(s), ph, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                const uint32_t as = a_col + (uint32_t)(s * G::kCols);
-#pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    const uint64_t bdesc = sw128_desc(st + j * kABytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t acc = (i | j | kk) != 0;
-                        if constexpr (kDequant) {
-                            mma_ts(tmem, as + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, acc);
-                            if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
-                                mma_ts(tmem, as + kLo + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, 1u);
-                        } else {
-                            const uint64_t adesc = sw128_desc(st + w_off);
-                            mma_ss(tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc, acc);
-                        }
-                    }
-                }
-                mma_commit(empty(s));
-                if (++s == S) { s = 0; ph ^= 1u; }
-            }
-            mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
-        }
-    } else {
-        if constexpr (EPI == EPI_W4A8) {
-            // the row factors, once per tile, while the first stages are in flight
-            for (int i = threadIdx.x - 64; i < BN; i += kEpiThreads) {
-                const int m = min(m_tile + i, p.M - 1);
-                const float as = __ldg(p.a_scale + m);
-                rowf[i] = make_float2(as, as * (float)__ldg(p.rowsum + m));
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-        }
-        // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each
-        // 64-wide sub-stage
-        const int q = warp & 3, h = (warp - 2) >> 2;
-        const int r = 32 * q + lane;                 // row inside the tile
-        const int row = n_tile + r;
-        const int rc = row < p.N ? row : p.N - 1;
-        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        if constexpr (kDequant) {
-            int s = 0;
-            uint32_t ph = 0;
-            int pos = (ks0 * SUB) % bpb;             // first sub-stage of the stage, within its K-block
-            for (int i = 0; i < nks; ++i) {
-                if (!mbar_wait(full_x(s), ph, abort_flag)) break;
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                uint32_t out[SUB][16], rest[SUB][16];
-#pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    uint4 raw[4];
-                    const uint32_t wsrc = st + w_off + r * (SUB * kRowB) + j * kRowB + h * (kRowB / 2);
-                    raw[0] = lds128u(wsrc);
-                    if constexpr (WF == WF_INT8) raw[1] = lds128u(wsrc + 16);
-                    float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and sub-stage
-                    if constexpr (G::kTable) {
-                        // K-block of the sub-stage in the box (the box starts at the stage's
-                        // first block); a sub-stage past K (its weights and activations read 0)
-                        // keeps the last block of the box
-                        const int d = (j == 0 || pos + j < bpb) ? 0 : min(1, p.tblocks - 1);
-                        e = lds64f(st + t_off + (r >> 4) * (p.tblocks * 128) + d * 128 + (r & 15) * 8);
-                    }
-                    convert32<WF, BF>(raw, e.y, e.x, out[j], rest[j]);
-                }
-                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t dst = a_col + lane_base + (uint32_t)(s * G::kCols) + 16 * h;
-#pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    tmem_st16(dst + 32 * j, out[j]);
-                    if constexpr (Split<WF, BF>::kOn) tmem_st16(dst + kLo + 32 * j, rest[j]);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(s));
-                if (++s == S) { s = 0; ph ^= 1u; }
-                if (SUB > 1 || bpb > 1) {
-                    pos += SUB;
-                    while (pos >= bpb) pos -= bpb;
-                }
-            }
-        }
-        // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
-        // The tile is written transposed into the (now idle) stage buffers as [m][128 n] and then
-        // copied out row by row with 16-byte stores.
-        const bool ok = mbar_wait(acc_full, 0u, abort_flag) && !*abort_flag;
-        tc_fence_after();
-        constexpr int kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2;
-        uint8_t* tile = smem;
-        if (ok) {
-            float ws = 0.f, wo = 0.f;
-            if constexpr (EPI == EPI_W4A8) {
-                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
-                wo = t.x;
-                ws = t.y;
-            }
-            // The fused epilogue: this thread's channel bias once, and per 32-column chunk the 32
-            // residual values (32 independent loads, one 64-byte segment of a residual row per
-            // warp each) before any of them is used; the activation is chosen once per chunk.
-            const bool has_ep = EPI != EPI_ACC && p.ep.any();
-            const bool has_res = has_ep && p.ep.residual != nullptr;
-            // the residual tile, when it came in by TMA, sits where this thread stages its outputs:
-            // each element is read and then overwritten by the same thread
-            const bool res_smem = has_res && p.r_tma && mbar_wait(res_full, 0u, abort_flag);
-            const bool res_glob = has_res && !p.r_tma;
-            const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
-            for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kAccCol + c0, v);
-                float rv[32];
-                if (res_glob) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int m = m_tile + c0 + i;
-                        rv[i] = (row < p.N && m < p.M) ? load_c<CDT>(p.ep.residual, (size_t)m * p.N + row) : 0.f;
-                    }
-                }
-                tmem_ld_wait();
-                if constexpr (EPI == EPI_ACC) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        reinterpret_cast<int32_t*>(tile)[(size_t)(c0 + i) * kBM + r] = __float2int_rn(__uint_as_float(v[i]));
-                } else {
-                    float y[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        y[i] = __uint_as_float(v[i]);
-                        if constexpr (EPI == EPI_W4A8) {
-                            // y is the exact integer accumulator (see the file comment):
-                            // as * (ws * acc + wo * rowsum) = ws * (as * acc) + wo * (as * rowsum)
-                            const float2 f = rowf[c0 + i];   // the same row for the whole warp: a broadcast
-                            y[i] = fmaf(ws, f.x * y[i], wo * f.y);
-                        }
-                    }
-                    if (has_ep) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) y[i] += bias_r;
-                        switch (p.ep.act) {
-                            case ACT_RELU:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_RELU>(y[i]);
-                                break;
-                            case ACT_SILU:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_SILU>(y[i]);
-                                break;
-                            case ACT_GELU_TANH:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_GELU_TANH>(y[i]);
-                                break;
-                            default: break;
-                        }
-                        if (res_glob) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) y[i] += rv[i];
-                        } else if (res_smem) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) y[i] += load_s<CDT>(tile, (size_t)(c0 + i) * kBM + r);
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) store_c<CDT>(tile, (size_t)(c0 + i) * kBM + r, y[i]);
-                }
-            }
-        }
-        if (p.c_tma) {
-            // one TMA store of the staged tile (rows and channels past the end are not written);
-            // the block may retire once the store has read shared memory
-            ptx::fence_proxy_async_smem();
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-            if (ok && threadIdx.x == 64) {
-                ptx::tma_store_3d(&maps.c, n_tile, m_tile, blockIdx.z, smem_u32(tile));
-                ptx::bulk_commit();
-                ptx::bulk_wait_read();
-            }
-        } else {
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-        if (ok) {
-            const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
-            constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
-            constexpr int kChunks = kBM / kPer;               // chunks per tile row
-            uint8_t* out = (EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C)) +
-                           (size_t)blockIdx.z * p.M * p.N * kEsz;
-            const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-            for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
-                const int ml = idx / kChunks, c = idx - ml * kChunks;
-                const int n0 = c * kPer;
-                if (n0 >= nvalid) continue;
-                const uint8_t* src = tile + ((size_t)ml * kBM + n0) * kEsz;
-                uint8_t* dst = out + ((size_t)(m_tile + ml) * p.N + n_tile + n0) * kEsz;
-                if (vec && n0 + kPer <= nvalid) {
-                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-                } else {
-                    for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
-                        for (int b = 0; b < kEsz; ++b) dst[e * kEsz + b] = src[e * kEsz + b];
-                }
-            }
-        }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// ---------------------------------------------------------------- W4A8 activation codes as f16
-__global__ void codes_to_f16_kernel(const int8_t* __restrict__ qa, __half* __restrict__ out, size_t n) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        out[i] = __int2half_rn(qa[i]);
-}
-
-// ---------------------------------------------------------------- host side
-// [M][K] 16-bit activations, box of 64 (K) x BN (rows), 128-byte swizzle; rows past M read 0.
-cudaError_t make_tmap(CUtensorMap* map, const void* A, bool bf16, int M, int K, int BN) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)BN};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                           const_cast<void*>(A), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// Rows of A per tile (the MMA's N): 64, 128 or 256.
-int pick_bn(int M) {
-    return M <= 64 ? 64 : (M <= 128 ? 128 : 256);
-}
-
-
-// The packed weight rows [N][row bytes] as a 2-D byte (quantized formats) or 16-bit (float mode,
-// 128-byte swizzle) tensor; box = one stage (sub sub-stages of 64) of 128 rows; rows past N and
-// bytes past K read 0.
-cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16, int N, int K, int sub) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    CUresult r;
-    if (wf == WF_FLOAT) {
-        const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(Bp),
-                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const int row_bytes = (wf == WF_INT8) ? K : K / 2;
-        const int box_bytes = sub * ((wf == WF_INT8) ? kBK : kBK / 2);
-        const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
-        const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-        const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kBM};
-        const cuuint32_t estr[2] = {1, 1};
-        r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Bp), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// The grouped {offset, scale} table [ceil(N/16)][nb][16][2] as a 2-D float tensor: x = 32 floats
-// per K-block of a group (16 channels x 2), y = group (stride nb * 128 bytes); box = tblocks
-// consecutive K-blocks of 8 groups (the tile's 128 channels); entries past the end read 0.
-cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int nb, int tblocks) {
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)32 * nb, (cuuint64_t)((N + 15) / 16)};
-    const cuuint64_t strides[1] = {(cuuint64_t)nb * 128};
-    const cuuint32_t box[2] = {(cuuint32_t)(32 * tblocks), (cuuint32_t)(kBM / 16)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(T), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// The output [depth][M][N] (bf16 / f16 / f32, or int32 accumulators; depth = the K-splits' partial
-// sums, else 1) as a 3-D tensor; box = one tile of 128 channels x BN rows of one slice, matching the
-// staged [rows][128] tile. Only when a row is a whole number of 16-byte units (TMA strides) and
-// the base is 16-byte aligned; else returns false.
-bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN, int depth) {
-    const size_t esz = kind == DT_F32 || kind < 0 ? 4 : 2;
-    if (((size_t)N * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return false;
-    EncodeTiledFn enc = tensor_map_encoder();
-    if (!enc) return false;
-    const CUtensorMapDataType dt = kind < 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32
-                                   : (kind == DT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                   : (kind == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16));
-    const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)depth};
-    const cuuint64_t strides[2] = {(cuuint64_t)N * esz, (cuuint64_t)M * N * esz};
-    const cuuint32_t box[3] = {(cuuint32_t)kBM, (cuuint32_t)BN, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int WF, bool BF, int EPI, int CDT, int BN>
-cudaError_t launch_k(const Maps& maps, const Params& p, cudaStream_t s) {
-    auto kern = prefill_kernel<WF, BF, EPI, CDT, BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
-    if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN, p.splits);
-    kern<<<grid, kThreads, kSmemMax, s>>>(maps, p);
-    return cudaGetLastError();
-}
-
-// The weight and table maps for the plan's sub-stages per stage, then the launch for the output
-// type c_dtype (EPI_ACC: int32).
-template <int WF, bool BF, int EPI, int BN>
-cudaError_t launch_bn(Maps maps, Params p, int c_dtype, cudaStream_t s) {
-    using P = Plan<WF, BF, BN>;
-    cudaError_t e = make_wmap(&maps.w, p.Bp, WF, BF, p.N, p.K, P::kSub);
-    if (e != cudaSuccess) return e;
-    p.tblocks = P::kSub < p.nb ? P::kSub : p.nb;
-    if constexpr (P::G::kTable) e = make_table_map(&maps.t, p.T, p.N, p.nb, p.tblocks);
-    else maps.t = maps.w;   // unused
-    if (e != cudaSuccess) return e;
-    if constexpr (EPI == EPI_ACC) return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
-    switch (c_dtype) {
-        case DT_F32: return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
-        case DT_F16: return launch_k<WF, BF, EPI, DT_F16, BN>(maps, p, s);
-        default: return launch_k<WF, BF, EPI, DT_BF16, BN>(maps, p, s);
-    }
-}
-
-template <int WF, bool BF, int EPI>
-cudaError_t launch_wf(const Maps& maps, const Params& p, int c_dtype, cudaStream_t s) {
-    switch (p.BN) {
-        case 64: return launch_bn<WF, BF, EPI, 64>(maps, p, c_dtype, s);
-        case 128: return launch_bn<WF, BF, EPI, 128>(maps, p, c_dtype, s);
-        default: return launch_bn<WF, BF, EPI, 256>(maps, p, c_dtype, s);
-    }
-}
-
-}  // namespace pf
 
 EncodeTiledFn tensor_map_encoder() {
     static EncodeTiledFn fn = nullptr;
@@ -881,6 +81,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.splits = a.splits > 1 ? a.splits : 1;
+    p.status = status_word_address();
+    if (!p.status) return cudaErrorInvalidValue;
     p.ep = p.splits > 1 ? Epilogue{} : a.ep;   // split partials: the reduction applies it
     // with K-splits the kernel writes float32 partial sums [splits][M][N], reduced in fixed order
     const int kdt = p.splits > 1 ? DT_F32 : a.c_dtype;
@@ -893,7 +95,13 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     if (!p.c_tma) maps.c = maps.a;             // unused
     p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), kdt, a.M, a.N, p.BN, 1) ? 1 : 0;
     if (!p.r_tma) maps.r = maps.a;             // unused
-    if (a.fmt == FMT_INT4)
+    if (prefill_codes_path(a.fmt, a.K, a.block, a.M, a.a_dtype)) {
+        // Int8-Block0: raw codes on the tensor cores, s * acc + o * sum_k a in the epilogue
+        e = launch_row_sums(a.M, a.K, a.A, a.a_dtype, a.rowsum, s);
+        if (e != cudaSuccess) return e;
+        p.rowsum_f = a.rowsum;
+        e = launch_prefill_codes8(maps, p, kdt, s);   // bf16 only
+    } else if (a.fmt == FMT_INT4)
         e = bf ? pf::launch_wf<pf::WF_INT4, true, pf::EPI_STORE>(maps, p, kdt, s)
                : pf::launch_wf<pf::WF_INT4, false, pf::EPI_STORE>(maps, p, kdt, s);
     else if (a.fmt == FMT_INT8)
@@ -904,33 +112,6 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
                : pf::launch_wf<pf::WF_FLOAT, false, pf::EPI_STORE>(maps, p, kdt, s);
     if (e != cudaSuccess || p.splits == 1) return e;
     return launch_splitk_reduce(a.partial, p.splits, (size_t)a.M * a.N, a.N, a.ep, a.C, a.c_dtype, s);
-}
-
-cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
-    pf::Params p{};
-    p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.K; p.nb = 1;
-    p.BN = pf::pick_bn(a.M);
-    p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
-    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc; p.splits = 1;
-    p.ep = a.acc ? Epilogue{} : a.ep;
-    pf::Maps maps;
-    cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
-    if (e != cudaSuccess) return e;
-    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN, 1) ? 1 : 0)
-                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN, 1) ? 1 : 0);
-    if (!p.c_tma) maps.c = maps.a;     // unused
-    p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), a.c_dtype, a.M, a.N, p.BN, 1)
-                  ? 1 : 0;
-    if (!p.r_tma) maps.r = maps.a;     // unused
-    if (a.acc) return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_ACC>(maps, p, DT_F32, s);
-    return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
-}
-
-cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s) {
-    const int threads = 256;
-    const size_t want = (n + threads - 1) / threads;
-    pf::codes_to_f16_kernel<<<(int)(want < 8192 ? want : 8192), threads, 0, s>>>(qa, static_cast<__half*>(out), n);
-    return cudaGetLastError();
 }
 
 }  // namespace qg

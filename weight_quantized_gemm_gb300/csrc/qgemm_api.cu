@@ -83,16 +83,23 @@ int prefill_splits_for(int M, int K, int N, int mode, size_t ws_bytes) {
     return splits;
 }
 
-// Scratch bytes of a call. The decode split-K partials and the W4A8 codes are required; the
-// tensor-core path's split-K partials are optional (with less scratch it splits less), so
-// `required` leaves them out.
+// Row-sum scratch of the tensor-core path for Int8-Block0 (float32 [M], 256-byte aligned), in
+// front of any split-K partials.
+size_t rowsum_ws(int M, int K, int mode, int block, int a_dtype) {
+    return qg::prefill_codes_path(fmt_of(mode), K, block, M, a_dtype) ? align256((size_t)M * sizeof(float)) : 0;
+}
+
+// Scratch bytes of a call. The decode split-K partials, the W4A8 codes and the Int8-Block0 row
+// sums are required; the tensor-core path's split-K partials are optional (with less scratch it
+// splits less), so `required` leaves them out.
 size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool required) {
     if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K);
     const Path path = choose_path(M, K, N, mode, a_dtype);
     if (path == PATH_PREFILL) {
-        if (required) return 0;
+        const size_t rows = rowsum_ws(M, K, mode, block, a_dtype);
+        if (required) return rows;
         const int splits = prefill_splits_for(M, K, N, mode, SIZE_MAX);
-        return splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+        return rows + (splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0);
     }
     if (path != PATH_DECODE) return 0;
     // the decode kernel runs 16 rows of A at a time; split-K partials are per 16-row launch
@@ -224,8 +231,12 @@ int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int
     const int fmt = fmt_of(mode);
     const Path path = choose_path(M, K, N, mode, a_dtype);
     if (path == PATH_PREFILL) {
-        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C, static_cast<float*>(workspace), 1, ep};
-        pa.splits = prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes : 0);
+        const size_t rows = rowsum_ws(M, K, mode, block, a_dtype);   // [row sums][split-K partials]
+        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C,
+                           rows ? reinterpret_cast<float*>(static_cast<char*>(workspace) + rows)
+                                : static_cast<float*>(workspace),
+                           1, ep, static_cast<float*>(workspace)};
+        pa.splits = prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes - rows : 0);
         e = qg::launch_prefill(pa, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
     }
