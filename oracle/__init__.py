@@ -70,6 +70,7 @@ def _load():
             "orc_w4a8_acc_points": [I64, P, P, I64, P, P, P],
             "orc_w4a8_out": [I64, I64, P, P, P, P, P],
             "orc_epilogue": [I64, I64, P, P, I, P],
+            "orc_w4a8_block_out": [I64, I64, I64, I64, P, P, P, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -254,6 +255,20 @@ def epilogue(R: np.ndarray, bias=None, act: int = ACT_NONE, residual=None) -> np
     return out
 
 
+def w4a8_block_out(qa: np.ndarray, s: np.ndarray, q: np.ndarray, T: np.ndarray, block: int) -> np.ndarray:
+    """W4A8 with block-quantized weights: as * sum_b (ws_b * block integer GEMM + off_b * block
+    row sum), float64. qa [M][K] int8, s [M], q [N][K] codes, T [N][K/block][2]."""
+    qa = np.ascontiguousarray(qa, dtype=np.int8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    T = np.ascontiguousarray(T, dtype=np.float32)
+    M, K = qa.shape
+    N = q.shape[0]
+    R = np.empty((M, N), dtype=np.float64)
+    _check(_load().orc_w4a8_block_out(M, K, N, block, _p(qa), _p(s), _p(q), _p(T), _p(R)), "w4a8_block_out")
+    return R
+
+
 # ---------------------------------------------------------------- whole layer
 QMAX = {1: 15, 2: 255, 3: 15}     # mode -> largest code (INT4, INT8, W4A8 weights)
 NBITS = {1: 4, 2: 8, 3: 4}
@@ -270,14 +285,18 @@ def reference_layer(mode: int, block: int, A_stored: np.ndarray, a_dtype: int, W
         out["Bp"] = Wt
         out["R"] = gemm(values(A_stored, a_dtype), values(Wt, w_dtype))
         return out
-    blk = K if (block == 0 or mode == 3) else block
+    blk = K if block == 0 else block
     q, T = quantize(W, blk, QMAX[mode])
     out.update(q=q, T=T, Bp=pack(q, NBITS[mode]))
     if mode == 3:
         A32 = values(A_stored, a_dtype).astype(np.float32)
         qa, s, rs = act_quant(A32)
-        acc = w4a8_acc(qa, q)
-        out.update(qa=qa, a_scale=s, rowsum=rs, acc=acc, R=w4a8_out(acc, s, rs, T))
+        out.update(qa=qa, a_scale=s, rowsum=rs)
+        if blk == K:   # per channel: one integer GEMM, rescaled per channel
+            acc = w4a8_acc(qa, q)
+            out.update(acc=acc, R=w4a8_out(acc, s, rs, T))
+        else:          # per K-block: integer GEMMs per block, rescaled per block
+            out.update(R=w4a8_block_out(qa, s, q, T, blk))
         return out
     out["R"] = gemm(values(A_stored, a_dtype), dequant(q, T, blk))
     return out

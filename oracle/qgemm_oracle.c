@@ -337,3 +337,32 @@ int orc_epilogue(int64_t M, int64_t N, double* R, const float* bias, int act, co
         }
     return ORC_OK;
 }
+
+/*
+ * W4A8 with weights quantized per K-block (the page's block sizes, «为什么用 Conv1x1 来测 GEMM»,
+ * applied to the W4A8 weights): each block b of K has its own {off_b, ws_b}, so the integer
+ * GEMM runs per block and the rescale sums the blocks:
+ *   R[m][n] = as[m] * sum_b (ws_b * sum_{k in b} qa q + off_b * sum_{k in b} qa)
+ * with the block sums in int64 and the rescale in double. q is [N][K], T is [N][K/block][2].
+ */
+int orc_w4a8_block_out(int64_t M, int64_t K, int64_t N, int64_t block, const int8_t* qa, const float* as,
+                       const uint8_t* q, const float* T, double* R) {
+    if (!qa || !as || !q || !T || !R || M <= 0 || K <= 0 || N <= 0 || block <= 0 || K % block) return ORC_ERR_ARG;
+    const int64_t nb = K / block;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double r = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                int64_t acc = 0, rs = 0;
+                for (int64_t k = b * block; k < (b + 1) * block; ++k) {
+                    acc += (int64_t)qa[m * K + k] * (int64_t)q[n * K + k];
+                    rs += qa[m * K + k];
+                }
+                const double off = (double)T[(n * nb + b) * 2 + 0], ws = (double)T[(n * nb + b) * 2 + 1];
+                r += ws * (double)acc + off * (double)rs;
+            }
+            R[m * N + n] = (double)as[m] * r;
+        }
+    return ORC_OK;
+}

@@ -237,9 +237,39 @@ def test_w4a8_exact_grid_equals_float_gemm():
     assert np.array_equal(pts, acc[[0, 8, 3], [12, 0, 5]])
 
 
+def test_w4a8_block_weights_pins():
+    """W4A8 with block-64 weights: on the exact activation grid the block rescale equals the float
+    GEMM of the dequantized block weights (a wrong block index, scale, offset or row sum fails
+    it); with one block over K it is the per-channel rescale exactly; a 2-row brute force in
+    Python integers checks the block sums."""
+    rng = np.random.default_rng(33)
+    M, K, N, blk = 7, 256, 11, 64
+    A_int = rng.integers(-127, 128, size=(M, K))
+    A_int[:, 5] = 127
+    A = (A_int * 2.0 ** -6).astype(np.float32)
+    W = synth.normal64(K * N, 8, 2, 0.02).astype(np.float32).reshape(K, N)
+    q, T = oracle.quantize(W, blk, 15)
+    qa, s, rs = oracle.act_quant(A)
+    assert np.array_equal(qa.astype(np.int64), A_int) and np.all(s == np.float32(2.0 ** -6))
+    R = oracle.w4a8_block_out(qa, s, q, T, blk)
+    ref = oracle.gemm(A.astype(np.float64), oracle.dequant(q, T, blk))
+    assert np.allclose(R, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    qK, TK = oracle.quantize(W, K, 15)
+    acc = oracle.w4a8_acc(qa, qK)
+    assert np.array_equal(oracle.w4a8_block_out(qa, s, qK, TK, K), oracle.w4a8_out(acc, s, rs, TK))
+    for m, n in [(0, 0), (6, 10)]:
+        tot = 0.0
+        for b in range(K // blk):
+            ks = range(b * blk, (b + 1) * blk)
+            a_q = sum(int(qa[m, k]) * int(q[n, k]) for k in ks)
+            r_s = sum(int(qa[m, k]) for k in ks)
+            tot += float(T[n, b, 1]) * a_q + float(T[n, b, 0]) * r_s
+        assert abs(R[m, n] - float(s[m]) * tot) <= 1e-12 * max(1.0, abs(R[m, n]))
+
+
 def test_reference_layer_modes_consistent():
     """The whole-layer helper wires the steps in the order the pages give."""
-    for mode, block in [(1, 64), (2, 0), (3, 0)]:
+    for mode, block in [(1, 64), (2, 0), (3, 0), (3, 64)]:
         w = synth.Workload("t", 5, 128, 24, mode, block, synth.BF16, synth.BF16, 1, 2)
         A = synth.make_activations(w)
         W = synth.make_weights(w)
