@@ -55,7 +55,7 @@ def algorithmic_bytes(w: synth.Workload, bias: bool = False, residual: bool = Fa
         tb = 0
     else:
         wb = w.K * w.N * (4 if w.mode in (synth.MODE_INT4, synth.MODE_W4A8) else 8) // 8
-        blk = w.K if (w.block == 0 or w.mode == synth.MODE_W4A8) else w.block
+        blk = w.K if w.block == 0 else w.block
         tb = w.N * (w.K // blk) * 8
     return wb + tb + w.M * w.K * esz[w.a_dtype] + w.M * w.N * esz[w.c_dtype] + extra
 
@@ -178,7 +178,7 @@ def oracle_step_fn(w: synth.Workload, A, W):
         rows = max(1, min(w.M, int(2e8 // (w.K * w.N))))
         return (lambda: oracle.gemm(A64[:rows], Bt)), rows, f"float GEMM of {rows} row(s) of A"
     qmax = oracle.QMAX[w.mode]
-    blk = w.K if (w.block == 0 or w.mode == synth.MODE_W4A8) else w.block
+    blk = w.K if w.block == 0 else w.block
     q, T = oracle.quantize(W, blk, qmax)       # offline step, not timed
     A64 = oracle.values(A, w.a_dtype)
     if w.mode == synth.MODE_W4A8:
@@ -187,6 +187,8 @@ def oracle_step_fn(w: synth.Workload, A, W):
 
         def run():
             qa, s, rs = oracle.act_quant(A32)
+            if blk != w.K:
+                return oracle.w4a8_block_out(qa, s, q, T, blk)
             return oracle.w4a8_out(oracle.w4a8_acc(qa, q), s, rs, T)
         return run, rows, f"W4A8 on {rows} row(s) of A"
     rows = max(1, min(w.M, int(4e8 // (w.K * w.N))))
@@ -418,6 +420,8 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--k", type=int, default=0, help="override the workload's K (e.g. the MNN shape grid)")
     ap.add_argument("--n", type=int, default=0, help="override the workload's N (e.g. the MNN shape grid)")
+    ap.add_argument("--block", type=int, default=-1,
+                    help="override the workload's K-block of the {offset, scale} table (0: per channel)")
     ap.add_argument("--a-dtype", default="", choices=["", "f16", "bf16", "f32"],
                     help="override the workload's activation dtype")
     ap.add_argument("--decode-max-m", type=int, default=0,
@@ -441,6 +445,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.a_dtype:
         w = dataclasses.replace(w, a_dtype={"f16": synth.F16, "bf16": synth.BF16, "f32": synth.F32}[args.a_dtype])
+    if args.block >= 0:
+        w = dataclasses.replace(w, block=args.block)
     if args.m or args.k or args.n:
         w = dataclasses.replace(w, M=args.m or w.M, K=args.k or w.K, N=args.n or w.N)
 

@@ -102,7 +102,8 @@ size_t qgemm_workspace_bytes(int M, int K, int N, int mode, int block, int a_dty
  * For each channel n and block b (block elements along K), in float32 round-to-nearest:
  *   lo = min w, hi = max w, scale = (hi - lo) / qmax, offset = lo,
  *   q = clamp(rint((w - lo) / scale), 0, qmax) with ties to even; q = 0 if scale == 0.
- * qmax = 15 for INT4 and W4A8, 255 for INT8. W4A8 requires block = 0 (per channel).
+ * qmax = 15 for INT4 and W4A8, 255 for INT8. W4A8 weights may be per channel (block = 0) or
+ * per K-block like INT4.
  * FLOAT mode instead writes W transposed to [N][K], rounded to nearest-even in w_dtype,
  * and T may be NULL. W must be finite. Writes Bp (qgemm_packed_bytes) and T
  * (qgemm_table_bytes). */
@@ -116,7 +117,10 @@ int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, v
  *   a_dtype: f32, f16 or bf16. FLOAT mode expects Bp in the same dtype as A.
  *   c_dtype: f32, f16 or bf16 (results are accumulated in f32 and rounded once).
  *   W4A8: A is quantized per row (as = max|a| / 127, qa = clamp(rint(a / as), -127, 127)),
- *   acc = sum_k qa * q in int32, and C = as * (ws * acc + off * sum_k qa).
+ *   acc = sum_k qa * q in int32, and C = as * (ws * acc + off * sum_k qa); with block-quantized
+ *   weights C = as * sum_b (ws_b * acc_b + off_b * sum_{k in b} qa) over the K-blocks b (the
+ *   weights are then dequantized per block to f16 for the tensor cores, so acc_b is not formed
+ *   exactly; the result is within the float bar).
  * Kernel choice is by shape only: f32 activations use an exact CUDA-core kernel; M <= 16
  * uses the weight-streaming decode kernel; larger M uses the tensor-core (tcgen05) kernel.
  * workspace may be NULL when qgemm_workspace_bytes() returns 0. M == 0 or N == 0 is a valid

@@ -62,7 +62,6 @@ FAKE = 1 << 40          # 16-byte aligned addresses that are never dereferenced 
     (dict(T=0), -1),
     (dict(C=FAKE + 8), -3),                 # misaligned
     (dict(Bp=FAKE + 1), -3),
-    (dict(mode=3, block=64), -2),           # W4A8 is per channel
     (dict(mode=3, block=0, ws=0, ws_bytes=0), -4),   # W4A8 needs scratch for the activation codes
     (dict(N=512, ws=0, ws_bytes=0), -4),    # small N: split-K scratch needed
     (dict(M=1 << 21), -2),                  # beyond the launch limit
@@ -90,7 +89,7 @@ def test_pack_and_aux_reject():
     assert lib.qgemm_pack(FAKE, 4096, 64, 1, 64, 0, FAKE, None, None) == -1          # null T
     assert lib.qgemm_pack(FAKE + 4, 4096, 64, 1, 64, 0, FAKE, FAKE, None) == -3      # misaligned W
     assert lib.qgemm_pack(FAKE, 4096, 64, 0, 0, 9, FAKE, None, None) == -1           # bad w_dtype
-    assert lib.qgemm_pack(FAKE, 4096, 64, 3, 64, 0, FAKE, FAKE, None) == -2          # W4A8 per channel
+    assert lib.qgemm_pack(FAKE, 4096, 64, 3, 96, 0, FAKE, FAKE, None) == -2          # block not a multiple of 64
     assert lib.qgemm_act_quant(4, 100, FAKE, 2, FAKE, FAKE, FAKE, None) == -2
     assert lib.qgemm_act_quant(4, 128, FAKE, 2, FAKE + 2, FAKE, FAKE, None) == -3
     assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, FAKE, 1 << 20, None) == -1

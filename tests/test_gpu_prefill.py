@@ -180,3 +180,16 @@ def test_w4a8_m2048_k4096_n14336_sampled():
     R = (s[mi].astype(np.float64) * (T[ni, 0, 1].astype(np.float64) * acc_ref.astype(np.float64) +
                                       T[ni, 0, 0].astype(np.float64) * rs[mi]))
     check_close(got[mi, ni], R, w.a_dtype, w.c_dtype, w.name)
+
+
+@pytest.mark.parametrize("M,K,N,block", [(1, 256, 40, 64), (40, 512, 96, 64), (300, 1024, 130, 128), (64, 2048, 256, 64)])
+@pytest.mark.parametrize("a_dtype", [synth.BF16, synth.F16])
+def test_w4a8_block_weights_layer(M, K, N, block, a_dtype):
+    """W4A8 with block-quantized weights against the oracle's per-block integer rescale."""
+    w, A_np, W_np = _w4a8_inputs(M, K, N, a_dtype)
+    ref = oracle.reference_layer(3, block, A_np, a_dtype, W_np)
+    Bp, T = gpu_pack(W_np, 3, block)
+    assert np.array_equal(Bp.cpu().numpy().reshape(N, -1), ref["Bp"])
+    assert np.array_equal(table_rows(T.cpu().numpy(), N, K // block), ref["T"])
+    got = gpu_run(M, K, N, 3, block, A_np, a_dtype, Bp, T, synth.BF16)
+    check_close(got, ref["R"], a_dtype, synth.BF16, f"w4a8 block {block}")

@@ -113,6 +113,7 @@ struct W4A8Args {
     void* C;        // rescaled output (or nullptr)
     int c_dtype;
     Epilogue ep;    // applied to the rescaled output
+    int block = 0;  // K-block of the weights' {offset, scale} (0 or K: per channel)
 };
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
 

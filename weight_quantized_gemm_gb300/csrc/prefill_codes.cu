@@ -20,7 +20,8 @@ cudaError_t launch_prefill_codes8(const pf::Maps& maps, const pf::Params& p, int
 
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     pf::Params p{};
-    p.M = a.M; p.K = a.K; p.N = a.N; p.block = a.K; p.nb = 1;
+    const int block = a.block > 0 ? a.block : a.K;
+    p.M = a.M; p.K = a.K; p.N = a.N; p.block = block; p.nb = a.K / block;
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
     p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc; p.splits = 1;
@@ -37,6 +38,13 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
                   ? 1 : 0;
     if (!p.r_tma) maps.r = maps.a;     // unused
     if (a.acc) return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_ACC>(maps, p, DT_F32, s);
+    if (block != a.K) {
+        // weights quantized per K-block: the block {offset, scale} vary along K, so the weights are
+        // dequantized per block into f16 (as on the Int4 path) and multiplied with the activation
+        // codes (exact f16 integers); the epilogue applies the row scale as only:
+        // as * sum_k qa (q s + o) = as * sum_b (s_b sum qa q + o_b sum qa)
+        return pf::launch_wf<pf::WF_INT4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
+    }
     return pf::launch_wf<pf::WF_CODES4, false, pf::EPI_W4A8>(maps, p, a.c_dtype, s);
 }
 

@@ -578,9 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (ok) {
             float ws = 0.f, wo = 0.f;
             if constexpr (EPI == EPI_W4A8) {
-                const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
-                wo = t.x;
-                ws = t.y;
+                if constexpr (G::kTable) {   // block-quantized W4A8 weights: dequantized per block already
+                    ws = 1.f;
+                    wo = 0.f;
+                } else {                     // raw codes: the per-channel {offset, scale} here
+                    const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
+                    wo = t.x;
+                    ws = t.y;
+                }
             }
             // The fused epilogue: this thread's channel bias once, and per 32-column chunk the 32
             // residual values (32 independent loads, one 64-byte segment of a residual row per

@@ -42,8 +42,6 @@ int check_shape(int K, int N, int mode, int* block) {
     if (mode == QGEMM_MODE_FLOAT) return QGEMM_OK;
     if (*block % 64 != 0 || K % *block != 0)
         return fail(QGEMM_ERR_UNSUPPORTED, "block %d must be a multiple of 64 dividing K=%d", *block, K);
-    if (mode == QGEMM_MODE_W4A8 && *block != K)
-        return fail(QGEMM_ERR_UNSUPPORTED, "W4A8 weights are per channel (block = K), got block %d", *block);
     return QGEMM_OK;
 }
 
@@ -223,7 +221,7 @@ int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int
         int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
         e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
         if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep};
+        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep, block};
         e = qg::launch_w4a8_gemm(w, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
     }
