@@ -55,14 +55,15 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
 int prefill_splits(int M, int K, int N, int fmt) {
     (void)fmt;
     // Mid-sized M leaves most SMs idle (one block per 128 channels x BN rows): split K across
-    // up to one wave of blocks, each split keeping at least kMinStages stages of 64. Tiles that
-    // already fill a third of a wave or more stay whole: two splits cost more in partial-sum
-    // traffic than they win (measured at 64 and 76 tiles).
+    // up to one wave of blocks, each split keeping at least kMinStages stages of 64. The split
+    // partial sums cost splits * M * N * 4 bytes of traffic: 256-row tiles that already fill a
+    // third of a wave or more stay whole (two splits measured slower at 64 and 76 tiles), smaller
+    // tiles split in two from half a wave down (measured faster at 76 tiles, M = 24..128).
     constexpr int kMinStages = 8;
     const int bn = pf::pick_bn(M);
     const long long tiles = (long long)((N + pf::kBM - 1) / pf::kBM) * ((M + bn - 1) / bn);
     long long splits = kTargetSms / tiles;
-    if (splits < 3) return 1;
+    if (splits < (bn >= 256 ? 3 : 2)) return 1;
     const int by_k = (K / pf::kBK) / kMinStages;
     if (splits > by_k) splits = by_k;
     return splits > 1 ? (int)splits : 1;
