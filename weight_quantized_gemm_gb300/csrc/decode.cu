@@ -1,6 +1,7 @@
 // Decode path (small M) host logic: K-split choice, 16-row launches, the fixed-order split-K
-// reduction, and the exact float32 CUDA-core kernel (float32 activations, any M). The
-// tensor-core weight-streaming kernel itself is in decode_kernel.cuh.
+// reduction (also used by the tensor-core path), and the exact float32 CUDA-core kernel (float32
+// activations, any M). The tensor-core weight-streaming kernels are in decode_stream.cuh (TMA-fed)
+// and decode_kernel.cuh (the other shapes).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

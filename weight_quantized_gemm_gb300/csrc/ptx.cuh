@@ -1,4 +1,4 @@
-// Inline-PTX building blocks shared by the TMA-fed kernels (prefill.cu, decode_stream.cuh):
+// Inline-PTX building blocks shared by the TMA-fed kernels (prefill_kernel.cuh, decode_stream.cuh):
 // mbarriers with bounded waits, tiled TMA loads and cp.async completion tracked by an mbarrier.
 #pragma once
 
