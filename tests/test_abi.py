@@ -139,3 +139,35 @@ def test_fused_epilogue_argument_checks():
     assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, FAKE + 4, 0, None, FAKE, 2, None, 0, None) == -3  # bias
     assert run(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, None, 0, FAKE + 2, FAKE, 2, None, 0, None) == -3  # residual
     assert run(0, 128, 8, 1, 64, None, 2, None, None, None, 3, None, None, 2, None, 0, None) == 0      # empty call
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    """No CPU fallback: with the compiled library absent, the binding raises instead of computing."""
+    monkeypatch.setattr(qg, "_lib", None)
+    monkeypatch.setattr(qg, "LIB_PATH", "/nonexistent/libqgemm.so")
+    with pytest.raises(ImportError):
+        qg.load()
+    with pytest.raises(ImportError):
+        qg.qgemm_workspace_bytes(64, 4096, 4096, qg.MODE_INT4, 64, qg.F16, qg.F16)
+
+
+@pytest.mark.parametrize("M", [17, 24, 64, 100, 128, 200, 256, 512, 1024])
+@pytest.mark.parametrize("K,N", [(1024, 4096), (2560, 1024), (4096, 2560), (2560, 9728), (9728, 2560), (4096, 14336)])
+def test_tensor_core_split_rule(M, K, N):
+    """The tensor-core path's K-split, read off the workspace size: the splits fill at most one
+    wave of 152 SMs, each keeps at least 8 stages of 64, 256-row tiles split 3 or more ways only,
+    and Int8-Block0 with bf16 and M >= 256 adds its row sums in front."""
+    bn = 64 if M <= 64 else (128 if M <= 128 else 256)
+    tiles = -(-N // 128) * -(-M // bn)
+    for mode, block, a_dtype in [(qg.MODE_INT4, 64, qg.F16), (qg.MODE_INT8, 0, qg.BF16), (qg.MODE_FLOAT, 0, qg.F16)]:
+        ws = qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, qg.BF16)
+        rows = -(-M * 4 // 256) * 256 if (mode == qg.MODE_INT8 and a_dtype == qg.BF16 and M >= 256) else 0
+        part = ws - rows
+        assert part % (M * N * 4) == 0
+        splits = part // (M * N * 4)
+        if splits:
+            assert 2 <= splits <= 152 // tiles and splits <= (K // 64) // 8
+            assert bn < 256 or 152 // tiles >= 3      # 256-row tiles: only when 3+ splits fit in a wave
+        else:
+            want = min(152 // tiles, (K // 64) // 8)
+            assert want < (3 if bn >= 256 else 2)
