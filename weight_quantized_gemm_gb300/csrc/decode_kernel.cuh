@@ -666,14 +666,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs p) {
 }
 
 // ---------------------------------------------------------------- dispatch
+// SMs of the device current at the first call (thread-safe one-time initialization).
 inline int sm_count() {
-    static int count = 0;
-    if (count == 0) {
-        int dev = 0;
+    static const int count = [] {
+        int dev = 0, n = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            count = kTargetSms;
-    }
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = kTargetSms;
+        return n;
+    }();
     return count;
 }
 

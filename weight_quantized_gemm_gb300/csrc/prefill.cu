@@ -10,14 +10,15 @@ namespace qg {
 __device__ unsigned int g_status_word;
 
 EncodeTiledFn tensor_map_encoder() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe one-time initialization); nullptr if the driver lacks it
+    static const EncodeTiledFn fn = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
+            return reinterpret_cast<EncodeTiledFn>(f);
+        return EncodeTiledFn(nullptr);
+    }();
     return fn;
 }
 
