@@ -1,19 +1,24 @@
 """Throughput of the weight-quantized linear layer on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--reps R] [--workload NAME] [--impl reference]
 
-One step is one call of the layer (qgemm_run) on the workload's synthetic inputs. The
-default workload is the decode GEMV of a 7B-class FFN up-projection: Int4-Block64 weights,
-M=1, K=4096, N=11008, bf16 activations and output. Its metric is the weight-stream
-bandwidth (the layer's algorithmic bytes: packed weights, {offset, scale} table,
-activations in, output out) and, beside it, TFLOPS = 2*M*K*N / t (the benchmark page's
-convention, "MNN GemmSpeed 基准测试实战" «测量流程»).
+One step is one call of the layer (qgemm_run) on the workload's synthetic inputs. The headline
+workload is the largest of the five: W4A8, M=2048, K=4096, N=14336 (per-channel INT4 weights,
+bf16 activations quantized per row to INT8, exact int32 sums, bf16 output), reported in TFLOPS =
+2*M*K*N / t (the benchmark page's convention, "MNN GemmSpeed 基准测试实战" «测量流程»). The same
+JSON line carries a per_config object with the other workloads: the Int4-Block64 small case
+(M=4, K=256, N=512, f32), the decode GEMV (M=1, K=4096, N=11008), Int8-Block0 at K=N=4096 for
+M in {1, 2, 4, 8, 16}, the Int4-Block64 prefill (M=1024, K=N=4096) and the fp16 GEMM beside W4A8;
+HBM-bound (M <= 16) workloads are reported in weight-stream GB/s (the layer's algorithmic bytes:
+packed weights, {offset, scale} table, activations in, output out), the others in TFLOPS.
 
-Timing: weights are packed once (offline, as on the page), then copied into enough
-rotating copies to exceed the L2 cache about 3x, so every call streams its weights from HBM.
-W warm-up calls, then exactly K calls captured in one CUDA graph and replayed between CUDA
-events on the launching stream, with a barrier and synchronize on both sides; the time is
-the max over ranks. GPU clocks are sampled with nvidia-smi during the timed region.
+Timing: weights are packed once (offline, as on the page), then copied into enough rotating
+copies (with the activations when M > 16) to exceed the L2 cache 3x, so every call streams from
+HBM. W warm-up calls, then K calls captured in one CUDA graph; the graph is replayed R times, each
+replay between CUDA events on the launching stream with a barrier and synchronize on both sides
+(max over ranks); the per-call time is the median replay / K (the minimum is reported beside it).
+The decode kernels are timed with and without programmatic dependent launch. GPU clocks are
+sampled with nvidia-smi during the headline's timed replays.
 
 --impl reference times the CPU oracle (float64 plain loops, the test suite's reference) on
 this host's cores on a bounded sample of the same workload; it is a deliberately slow
@@ -40,7 +45,7 @@ sys.path.insert(0, ROOT)
 from weight_quantized_gemm_gb300 import synth  # noqa: E402
 
 METRIC = "qGEMM TFLOPS (2*M*K*N/s) and weight-stream HBM GB/s, % of roofline"
-DEFAULT_WORKLOAD = "int4_b64_decode_m1_k4096_n11008_bf16"
+HEADLINE_WORKLOAD = "w4a8_m2048_k4096_n14336"
 DTYPE_NAME = {0: "f32", 1: "f16", 2: "bf16"}
 
 
@@ -253,123 +258,228 @@ def to_torch(arr: np.ndarray, code: int, device):
 ACTS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 
 
-def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
-    import torch
+class Layer:
+    """One workload on the GPU: packed weights in enough rotating copies (and, for M > 16,
+    activations) to exceed the L2 cache 3x, so that every call streams from HBM."""
 
-    import weight_quantized_gemm_gb300 as qg
-    if args.decode_max_m:
-        qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, args.decode_max_m)
-    if args.no_split_k:
-        qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
-    device = torch.device("cuda", torch.cuda.current_device())
-    stream = torch.cuda.Stream(device)
-    tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
-    A_np = synth.make_activations(w)
-    W_np = synth.make_weights(w)
-    K, N, M = w.K, w.N, w.M
-    with torch.cuda.stream(stream):
-        A = to_torch(A_np, w.a_dtype, device)
-        Wd = torch.from_numpy(W_np).to(device)
-        pb = qg.qgemm_packed_bytes(K, N, w.mode, w.w_dtype if w.mode == 0 else 0)
-        tb = qg.qgemm_table_bytes(K, N, w.mode, w.block)
-        Bp0 = torch.empty(pb, dtype=torch.uint8, device=device)
-        T0 = torch.empty(max(tb // 4, 4), dtype=torch.float32, device=device)
-        qg.qgemm_pack(Wd, K, N, w.mode, w.block, w.a_dtype if w.mode == 0 else 0, Bp0, T0 if tb else None,
-                      stream=stream)
-        del Wd
-        l2 = torch.cuda.get_device_properties(device).L2_cache_size
-        copy_bytes = pb + tb
-        a_bytes = A.numel() * A.element_size() if M > 16 else 0
-        copies = max(2, -(-3 * l2 // max(copy_bytes + a_bytes, 1)))
-        Bps = [Bp0] + [Bp0.clone() for _ in range(copies - 1)]
-        Ts = [T0] + [T0.clone() for _ in range(copies - 1)]
-        # for M > 16 the activations are large too: rotate them with the weights
-        As = [A] + ([A.clone() for _ in range(copies - 1)] if M > 16 else [])
-        C = torch.empty((M, N), dtype=tdt[w.c_dtype], device=device)
-        wsb = qg.qgemm_workspace_bytes(M, K, N, w.mode, w.block, w.a_dtype, w.c_dtype)
-        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
-        # the fused epilogue's inputs (qgemm_run_fused), when asked for
-        bias = (torch.from_numpy(synth.normal64(N, 11, stream=4, std=0.5).astype(np.float32)).to(device)
-                if args.bias else None)
-        res = (to_torch(synth.encode(synth.normal64(M * N, 12, stream=5).reshape(M, N), w.c_dtype), w.c_dtype, device)
-               if args.residual else None)
-    stream.synchronize()
-    s_ptr = stream.cuda_stream
-    lib = qg.load()
-    act = ACTS[args.act]
-    fused = bias is not None or res is not None or act != 0
+    def __init__(self, w: synth.Workload, device, stream, bias=False, residual=False, act="none"):
+        import torch
 
-    def call(i):
-        if fused:
-            rc = lib.qgemm_run_fused(M, K, N, w.mode, w.block, As[i % len(As)].data_ptr(), w.a_dtype,
-                                     Bps[i % copies].data_ptr(), Ts[i % copies].data_ptr() if tb else None,
-                                     None if bias is None else bias.data_ptr(), act,
-                                     None if res is None else res.data_ptr(), C.data_ptr(), w.c_dtype,
-                                     ws.data_ptr(), wsb, s_ptr)
-        else:
-            rc = lib.qgemm_run(M, K, N, w.mode, w.block, As[i % len(As)].data_ptr(), w.a_dtype,
-                               Bps[i % copies].data_ptr(), Ts[i % copies].data_ptr() if tb else None, C.data_ptr(),
-                               w.c_dtype, ws.data_ptr(), wsb, s_ptr)
-        if rc != 0:
-            raise qg.QgemmError(rc, "qgemm_run")
-
-    # kernels per call: W4A8 = activation quantization + GEMM; otherwise one GEMM launch per
-    # 16-row decode launch (or one tensor-core launch), plus the split-K reduction when the call
-    # splits K (its workspace holds the partial sums)
-    if w.mode == synth.MODE_W4A8:
-        launches_per_call = 2
-    else:
-        decode_path = w.a_dtype != synth.F32 and M <= (args.decode_max_m or 16)
-        launches_per_call = (-(-M // 16) if decode_path else 1) * (2 if wsb > 0 else 1)
-    # warm-up (eager), then one CUDA graph of exactly K calls per launch mode: plain stream
-    # order, and with QGEMM_OPT_LAUNCH_OVERLAP (each decode call may start while the previous
-    # one finishes; it prefetches weights and waits for the previous kernel before A and C).
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            call(i)
-    stream.synchronize()
-    graphs = {}
-    for mode in (0, 1):
-        qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, mode)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(args.steps):
-                call(i)
-        graphs[mode] = g
-    qg.qgemm_set_option(qg.OPT_LAUNCH_OVERLAP, 0)
-    stream.synchronize()
-
-    def timed(g):
-        g.replay()          # one untimed replay: the graph's own first-launch cost stays out
+        import weight_quantized_gemm_gb300 as qg
+        self.w, self.device, self.stream = w, device, stream
+        self.qg, self.lib = qg, qg.load()
+        tdt = {0: torch.float32, 1: torch.float16, 2: torch.bfloat16}
+        K, N, M = w.K, w.N, w.M
+        with torch.cuda.stream(stream):
+            A = to_torch(synth.make_activations(w), w.a_dtype, device)
+            Wd = torch.from_numpy(synth.make_weights(w)).to(device)
+            self.pb = qg.qgemm_packed_bytes(K, N, w.mode, w.w_dtype if w.mode == 0 else 0)
+            self.tb = qg.qgemm_table_bytes(K, N, w.mode, w.block)
+            Bp0 = torch.empty(self.pb, dtype=torch.uint8, device=device)
+            T0 = torch.empty(max(self.tb // 4, 4), dtype=torch.float32, device=device)
+            qg.qgemm_pack(Wd, K, N, w.mode, w.block, w.a_dtype if w.mode == 0 else 0, Bp0,
+                          T0 if self.tb else None, stream=stream)
+            del Wd
+            self.l2 = torch.cuda.get_device_properties(device).L2_cache_size
+            a_bytes = A.numel() * A.element_size() if M > 16 else 0
+            self.copy_bytes = self.pb + self.tb
+            self.copies = max(2, -(-3 * self.l2 // max(self.copy_bytes + a_bytes, 1)))
+            self.Bps = [Bp0] + [Bp0.clone() for _ in range(self.copies - 1)]
+            self.Ts = [T0] + [T0.clone() for _ in range(self.copies - 1)]
+            self.As = [A] + ([A.clone() for _ in range(self.copies - 1)] if M > 16 else [])
+            self.C = torch.empty((M, N), dtype=tdt[w.c_dtype], device=device)
+            self.wsb = qg.qgemm_workspace_bytes(M, K, N, w.mode, w.block, w.a_dtype, w.c_dtype)
+            self.ws = torch.empty(max(self.wsb, 16), dtype=torch.uint8, device=device)
+            self.bias = (torch.from_numpy(synth.normal64(N, 11, stream=4, std=0.5).astype(np.float32)).to(device)
+                         if bias else None)
+            self.res = (to_torch(synth.encode(synth.normal64(M * N, 12, stream=5).reshape(M, N), w.c_dtype),
+                                 w.c_dtype, device) if residual else None)
+            # the activation pass alone (W4A8): same rows, codes written as int8
+            if w.mode == synth.MODE_W4A8:
+                self.qa = torch.empty((M, K), dtype=torch.int8, device=device)
+                self.asc = torch.empty(M, dtype=torch.float32, device=device)
+                self.rsum = torch.empty(M, dtype=torch.int32, device=device)
         stream.synchronize()
+        self.act = ACTS[act]
+        self.fused = self.bias is not None or self.res is not None or self.act != 0
+
+    def launches_per_call(self, decode_max_m: int) -> int:
+        """This library's kernels per call: W4A8 = activation quantization + GEMM; otherwise one
+        launch per 16-row decode launch (or one tensor-core launch), plus the split-K reduction."""
+        w = self.w
+        if w.mode == synth.MODE_W4A8:
+            return 2
+        decode_path = w.a_dtype != synth.F32 and w.M <= decode_max_m
+        return (-(-w.M // 16) if decode_path else 1) * (2 if self.wsb > 0 else 1)
+
+    def call(self, i: int):
+        w, lib, s_ptr = self.w, self.lib, self.stream.cuda_stream
+        A, Bp = self.As[i % len(self.As)].data_ptr(), self.Bps[i % self.copies].data_ptr()
+        T = self.Ts[i % self.copies].data_ptr() if self.tb else None
+        if self.fused:
+            rc = lib.qgemm_run_fused(w.M, w.K, w.N, w.mode, w.block, A, w.a_dtype, Bp, T,
+                                     None if self.bias is None else self.bias.data_ptr(), self.act,
+                                     None if self.res is None else self.res.data_ptr(), self.C.data_ptr(), w.c_dtype,
+                                     self.ws.data_ptr(), self.wsb, s_ptr)
+        else:
+            rc = lib.qgemm_run(w.M, w.K, w.N, w.mode, w.block, A, w.a_dtype, Bp, T, self.C.data_ptr(), w.c_dtype,
+                               self.ws.data_ptr(), self.wsb, s_ptr)
+        if rc != 0:
+            raise self.qg.QgemmError(rc, "qgemm_run")
+
+    def act_quant_call(self, i: int):
+        w = self.w
+        rc = self.lib.qgemm_act_quant(w.M, w.K, self.As[i % len(self.As)].data_ptr(), w.a_dtype, self.qa.data_ptr(),
+                                      self.asc.data_ptr(), self.rsum.data_ptr(), self.stream.cuda_stream)
+        if rc != 0:
+            raise self.qg.QgemmError(rc, "qgemm_act_quant")
+
+    def graph(self, fn, calls: int, overlap: int):
+        import torch
+        self.qg.qgemm_set_option(self.qg.OPT_LAUNCH_OVERLAP, overlap)
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(calls):
+                    fn(i)
+        finally:
+            self.qg.qgemm_set_option(self.qg.OPT_LAUNCH_OVERLAP, 0)
+        return g
+
+
+def time_graph(g, stream, reps: int, dist, device) -> list[float]:
+    """Milliseconds of each of `reps` replays of graph g, each replay bracketed by a barrier and a
+    synchronize on both sides and timed with CUDA events on the launching stream (max over
+    ranks). One untimed replay first keeps the graph's own first-launch cost out."""
+    import torch
+    g.replay()
+    stream.synchronize()
+    out = []
+    for _ in range(reps):
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            g.replay()
-            end.record(stream)
+        start.record(stream)
+        g.replay()
+        end.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        return max_over_ranks(start.elapsed_time(end), dist, device)
+        out.append(max_over_ranks(start.elapsed_time(end), dist, device))
+    return out
 
-    ms_plain = timed(graphs[0])
+
+def per_call(ms_list: list[float], calls: int) -> dict:
+    return {"median_ms": statistics.median(ms_list) / calls, "min_ms": min(ms_list) / calls}
+
+
+def roofline_of(w: synth.Workload, call_ms: float, peaks: dict, alg: int, kernel_ms: float | None = None) -> dict:
+    bound = bound_of(w)
+    t = (kernel_ms if kernel_ms is not None else call_ms) / 1e3
+    if bound == "hbm":
+        achieved, peak, unit, src = alg / t / 1e9, peaks["hbm_gbs"], "GB/s", "hbm_gbs"
+    else:
+        achieved, peak, unit, src = w.flops / t / 1e12, peaks["bf16_tflops"], "TFLOP/s", "bf16_tflops"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_source": f"{peaks['source']} ({src})", "traffic": measured_traffic(w), "algorithmic_bytes": alg,
+            "kernel": kernel_of(w)}
+
+
+def metric_value(w: synth.Workload, step_s: float, alg: int, world: int = 1) -> tuple[float, str]:
+    if bound_of(w) == "hbm":
+        return job_rate(alg, step_s, world) / 1e9, "GB/s"
+    return job_rate(w.flops, step_s, world) / 1e12, "TFLOP/s"
+
+
+def calls_for(layer: Layer, min_ms: float = 1.0, cap: int = 4000) -> int:
+    """Calls per graph so that one replay lasts at least min_ms (from a short eager estimate)."""
+    import torch
+    for i in range(3):
+        layer.call(i)
+    s = layer.stream
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s)
+    for i in range(10):
+        layer.call(i)
+    end.record(s)
+    s.synchronize()
+    est = max(start.elapsed_time(end) / 10, 1e-3)
+    return int(min(cap, max(20, -(-min_ms // est))))
+
+
+def bench_entry(w: synth.Workload, device, stream, peaks: dict, reps: int, dist, decode_max_m: int,
+                cpu_seconds: float, rank: int) -> dict:
+    """One per-config line: median / min per-call time over `reps` replays of a graph of calls
+    lasting >= 1 ms, with and without launch overlap for the decode kernels, its roofline and
+    the oracle timed on a bounded sample."""
+    layer = Layer(w, device, stream)
+    calls = calls_for(layer)
+    alg = algorithmic_bytes(w)
+    modes = (1, 0) if kernel_of(w) == "decode" else (0,)
+    out = {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "mode": synth.MODE_NAMES[w.mode],
+           "a_dtype": DTYPE_NAME[w.a_dtype], "c_dtype": DTYPE_NAME[w.c_dtype], "calls_per_replay": calls,
+           "replays": reps}
+    for mode in modes:
+        g = layer.graph(layer.call, calls, mode)
+        t = per_call(time_graph(g, stream, reps, dist, device), calls)
+        del g
+        value, unit = metric_value(w, t["median_ms"] / 1e3, alg)
+        key = "" if mode == modes[0] else "_no_overlap"
+        out["ms_per_step" + key] = t["median_ms"]
+        out["ms_per_step_min" + key] = t["min_ms"]
+        out["value" + key] = value
+        out["unit"] = unit
+        if mode == modes[0]:
+            out["launch_overlap"] = bool(mode)
+            out["roofline"] = roofline_of(w, t["median_ms"], peaks, alg)
+            out["tflops"] = w.flops / (t["median_ms"] / 1e3) / 1e12
+            out["gbs"] = alg / (t["median_ms"] / 1e3) / 1e9
+    if rank == 0 and cpu_seconds > 0:
+        ref = run_reference(argparse.Namespace(steps=10 ** 6, warmup=1, cpu_seconds=cpu_seconds), w)
+        out["cpu_baseline"] = {"value": ref["value"] if bound_of(w) == "hbm" else ref["tflops"],
+                               "unit": "GB/s" if bound_of(w) == "hbm" else "TFLOP/s", "cores": ref["cores"],
+                               "kind": "oracle", "sample": ref["sample"]}
+    del layer
+    return out
+
+
+def run_headline(args, w: synth.Workload, device, stream, peaks: dict, dist, world: int) -> dict:
+    """The headline workload: K calls in one CUDA graph, replayed `reps` times (median and min
+    per call), clocks sampled during the timed replays, the end-to-end rate through the public
+    binding with host buffers, and (W4A8) the activation pass timed alone."""
+    import torch
+    layer = Layer(w, device, stream, bias=args.bias, residual=args.residual, act=args.act)
+    decode = kernel_of(w) == "decode"
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            layer.call(i)
+    stream.synchronize()
+    graphs = {m: layer.graph(layer.call, args.steps, m) for m in ((1, 0) if decode else (0,))}
+    main_mode = 1 if decode else 0
+    res = {}
+    if decode:
+        res["plain"] = per_call(time_graph(graphs[0], stream, args.reps, dist, device), args.steps)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         t_wall = time.perf_counter()
-        ms = timed(graphs[1])
+        res["main"] = per_call(time_graph(graphs[main_mode], stream, args.reps, dist, device), args.steps)
         t_wall = time.perf_counter() - t_wall
         if t_wall < 1.0:    # keep the sampler running long enough to see the load (replays are identical)
-            with torch.cuda.stream(stream):
-                for _ in range(min(int(1.0 / max(t_wall, 1e-4)), 2000)):
-                    graphs[1].replay()
+            for _ in range(min(int(1.0 / max(t_wall / args.reps, 1e-5)), 5000)):
+                graphs[main_mode].replay()
             stream.synchronize()
-    clocks = clk.summary()
+    res["clocks"] = clk.summary()
+    if w.mode == synth.MODE_W4A8:
+        g = layer.graph(layer.act_quant_call, args.steps, 0)
+        res["act_quant"] = per_call(time_graph(g, stream, args.reps, dist, device), args.steps)
+        del g
+    del graphs
 
-    # end to end through the public API with host buffers: H2D of A, the call, D2H of C, per step
+    # end to end through the public binding with host buffers: H2D of A, the call, D2H of C, per step
+    qg = layer.qg
+    A, C = layer.As[0], layer.C
     A_host = A.cpu().pin_memory()
     C_host = torch.empty(C.shape, dtype=C.dtype).pin_memory()
     e2e_steps = max(1, min(args.steps, 300))
@@ -378,14 +488,16 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, dist) -> dict:
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
             A.copy_(A_host, non_blocking=True)
-            qg.qgemm_run(M, K, N, w.mode, w.block, A, w.a_dtype, Bps[i % copies], Ts[i % copies] if tb else None, C,
-                         w.c_dtype, ws if wsb else None, wsb, stream=stream)
+            qg.qgemm_run(w.M, w.K, w.N, w.mode, w.block, A, w.a_dtype, layer.Bps[i % layer.copies],
+                         layer.Ts[i % layer.copies] if layer.tb else None, C, w.c_dtype,
+                         layer.ws if layer.wsb else None, layer.wsb, stream=stream)
             C_host.copy_(C, non_blocking=True)
             stream.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    return {"ms": ms, "ms_plain": ms_plain, "clocks": clocks, "copies": copies, "copy_bytes": copy_bytes, "l2": l2,
-            "launches_per_call": launches_per_call, "e2e_s": e2e_s,
-            "h2d": A.numel() * A.element_size(), "d2h": C.numel() * C.element_size()}
+    res["e2e_s"] = (time.perf_counter() - t0) / e2e_steps
+    res.update(copies=layer.copies, copy_bytes=layer.copy_bytes, l2=layer.l2,
+               launches_per_call=layer.launches_per_call(args.decode_max_m or 16),
+               h2d=A.numel() * A.element_size(), d2h=C.numel() * C.element_size())
+    return res
 
 
 def profile_calls(w: synth.Workload, calls: int) -> dict:
@@ -411,12 +523,26 @@ def profile_calls(w: synth.Workload, calls: int) -> dict:
     return {"workload": w.name, "M": w.M, "calls": calls, "status": qg.qgemm_status()}
 
 
+# the workloads measured beside the headline (one GPU each, the same JSON line)
+PER_CONFIG = [
+    ("int4_b64_m4_k256_n512_f32", None),
+    ("int4_b64_decode_m1_k4096_n11008_bf16", None),
+    *[("int8_b0_k4096_n4096_f16", m) for m in synth.INT8_M_SWEEP],
+    ("int4_b64_prefill_m1024_k4096_n4096", None),
+    ("float_f16_m2048_k4096_n14336", None),
+]
+
+
 def main():
+    import dataclasses
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--steps", type=int, default=20, help="calls per timed CUDA graph (the K of the contract)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=25, help="timed replays of the graph (the median is reported)")
+    ap.add_argument("--workload", default=HEADLINE_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--per-config", choices=["auto", "on", "off"], default="auto",
+                    help="also measure the other workloads into a per_config object (auto: with the headline)")
     ap.add_argument("--m", type=int, default=0, help="override the workload's M (e.g. the Int8-Block0 M sweep)")
     ap.add_argument("--k", type=int, default=0, help="override the workload's K (e.g. the MNN shape grid)")
     ap.add_argument("--n", type=int, default=0, help="override the workload's N (e.g. the MNN shape grid)")
@@ -434,6 +560,7 @@ def main():
     ap.add_argument("--residual", action="store_true", help="fused epilogue: add a residual [M][N]")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="oracle budget of the headline's cpu_baseline")
     ap.add_argument("--print-src-hash", action="store_true", help="print the dominant kernel's source hash and exit")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="pack, run this many plain calls of the layer, print a status line and exit "
@@ -441,7 +568,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    import dataclasses
+    if args.reps < 1:
+        ap.error("--reps must be >= 1")
     w = synth.WORKLOADS[args.workload]
     if args.a_dtype:
         w = dataclasses.replace(w, a_dtype={"f16": synth.F16, "bf16": synth.BF16, "f32": synth.F32}[args.a_dtype])
@@ -449,6 +577,10 @@ def main():
         w = dataclasses.replace(w, block=args.block)
     if args.m or args.k or args.n:
         w = dataclasses.replace(w, M=args.m or w.M, K=args.k or w.K, N=args.n or w.N)
+    fused = args.bias or args.residual or args.act != "none"
+    headline_default = (args.workload == HEADLINE_WORKLOAD and not (args.m or args.k or args.n or args.a_dtype)
+                        and args.block < 0 and not fused)
+    per_config = args.per_config == "on" or (args.per_config == "auto" and headline_default)
 
     if args.print_src_hash:
         print(kernel_of(w), src_hash(kernel_of(w)))
@@ -456,23 +588,27 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     peaks = load_peaks()
-    base_config = {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "mode": synth.MODE_NAMES[w.mode],
-                   "block": w.block if w.block else w.K, "a_dtype": DTYPE_NAME[w.a_dtype],
-                   "c_dtype": DTYPE_NAME[w.c_dtype]}
-    if args.bias or args.residual or args.act != "none":
-        base_config["epilogue"] = {"bias": args.bias, "act": args.act, "residual": args.residual}
+    config = {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "mode": synth.MODE_NAMES[w.mode],
+              "block": w.block if w.block else w.K, "a_dtype": DTYPE_NAME[w.a_dtype],
+              "c_dtype": DTYPE_NAME[w.c_dtype]}
+    if fused:
+        config["epilogue"] = {"bias": args.bias, "act": args.act, "residual": args.residual}
+    bound = bound_of(w)
+    unit = "GB/s" if bound == "hbm" else "TFLOP/s"
+    dtype = "s8" if w.mode == synth.MODE_W4A8 else DTYPE_NAME[w.a_dtype]
 
     if args.impl == "reference":
         if rank != 0:
             return
         r = run_reference(args, w)
-        line = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": r["unit"], "n_gpus": args.gpus,
+        value = r["value"] if bound == "hbm" else r["tflops"]
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
                 "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": base_config, "tflops": r["tflops"],
-                "cpu_baseline": {"value": r["value"], "unit": r["unit"], "cores": r["cores"], "kind": "oracle",
+                "data": "synthetic", "config": config, "tflops": r["tflops"],
+                "cpu_baseline": {"value": value, "unit": unit, "cores": r["cores"], "kind": "oracle",
                                  "sample": r["sample"]},
-                "e2e": {"value": r["value"], "unit": r["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
@@ -487,44 +623,75 @@ def main():
         torch.cuda.set_device(local)
         dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
         dist = dist_mod
-    r = run_gpu(args, w, rank, world, dist)
-    step_s = r["ms"] / 1e3 / args.steps
+    import weight_quantized_gemm_gb300 as qg
+    if args.decode_max_m:
+        qg.qgemm_set_option(qg.OPT_DECODE_MAX_M, args.decode_max_m)
+    if args.no_split_k:
+        qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device)
+
+    r = run_headline(args, w, device, stream, peaks, dist, world)
+    step_s = r["main"]["median_ms"] / 1e3
     alg = algorithmic_bytes(w, args.bias, args.residual)
-    gbs = job_rate(alg, step_s, world) / 1e9
-    tflops = job_rate(w.flops, step_s, world) / 1e12
-    bound = bound_of(w)
-    if bound == "hbm":
-        achieved, peak, unit = alg / step_s / 1e9, peaks["hbm_gbs"], "GB/s"
-    else:
-        achieved, peak, unit = w.flops / step_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    value, _ = metric_value(w, step_s, alg, world)
+    # the dominant kernel's time: W4A8 calls are the activation pass plus the GEMM; the GEMM's
+    # share is the call time less the activation pass timed alone in its own graph
+    kernel_ms = None
+    if w.mode == synth.MODE_W4A8:
+        kernel_ms = r["main"]["median_ms"] - r["act_quant"]["median_ms"]
+    roof = roofline_of(w, r["main"]["median_ms"], peaks, alg, kernel_ms)
+    if kernel_ms is not None:
+        roof["kernel"] = "prefill (W4A8 GEMM; time = call - activation pass alone)"
+        whole = roofline_of(w, r["main"]["median_ms"], peaks, alg)
+        roof["whole_call"] = {"achieved": whole["achieved"], "frac": whole["frac"],
+                              "ms": r["main"]["median_ms"]}
     line = {
-        "metric": METRIC, "value": gbs if bound == "hbm" else tflops, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[w.a_dtype],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded SplitMix64/Box-Muller inputs of the workload's shape)",
-        "config": dict(base_config, parallelism=f"replicas x{world}",
-                       l2=f"{r['copies']} rotating copies of the weights ({r['copy_bytes'] / 1e6:.1f} MB)"
-                          f"{' and activations' if w.M > 16 else ''} (> 3x the {r['l2'] / 1e6:.0f} MB L2)",
-                       timing=f"CUDA graph of {args.steps} back-to-back calls, CUDA events",
-                       launch_overlap="QGEMM_OPT_LAUNCH_OVERLAP=1 (programmatic dependent launch)"),
-        "tflops": tflops, "gbs": gbs,
-        "ms_per_step_no_overlap": r["ms_plain"] / args.steps,
-        "value_no_overlap": (job_rate(alg, r["ms_plain"] / 1e3 / args.steps, world) / 1e9) if bound == "hbm"
-        else (job_rate(w.flops, r["ms_plain"] / 1e3 / args.steps, world) / 1e12),
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "peak_source": f"{peaks['source']} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-                     "traffic": measured_traffic(w), "algorithmic_bytes": alg,
-                     "kernel": kernel_of(w)},
-        "clocks": r["clocks"], "gpu_launches": args.steps * r["launches_per_call"],
-        "e2e": {"value": (alg / r["e2e_s"] / 1e9) if bound == "hbm" else (w.flops / r["e2e_s"] / 1e12),
-                "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "ms_per_step": r["e2e_s"] * 1e3,
+        "config": config,
+        "setup": {"parallelism": f"replicas x{world}",
+                  "l2": f"{r['copies']} rotating copies of the weights ({r['copy_bytes'] / 1e6:.1f} MB)"
+                        f"{' and activations' if w.M > 16 else ''} (> 3x the {r['l2'] / 1e6:.0f} MB L2)",
+                  "timing": f"CUDA graph of {args.steps} back-to-back calls, {args.reps} timed replays "
+                            f"(CUDA events, barrier + synchronize around each); ms_per_step = median replay / "
+                            f"{args.steps}",
+                  "launch_overlap": ("QGEMM_OPT_LAUNCH_OVERLAP=1 (programmatic dependent launch); "
+                                     "value_no_overlap without it") if kernel_of(w) == "decode" else "n/a",
+                  "dtype": ("int8 activation codes x 4-bit weight codes, exact int32 sums (f16 tensor "
+                            "cores, every partial sum an exact integer)") if w.mode == synth.MODE_W4A8 else
+                           f"{DTYPE_NAME[w.a_dtype]} activations, float32 accumulation"},
+        "ms_per_step_min": r["main"]["min_ms"],
+        "tflops": w.flops / step_s / 1e12 * world, "gbs": alg / step_s / 1e9 * world,
+        "roofline": roof, "clocks": r["clocks"],
+        "gpu_launches": args.steps * r["launches_per_call"] * args.reps,
+        "gpu_launches_per_step": r["launches_per_call"],
+        "e2e": {"value": metric_value(w, r["e2e_s"], alg, world)[0], "unit": unit, "ms_per_step": r["e2e_s"] * 1e3,
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
+    if "plain" in r:
+        line["ms_per_step_no_overlap"] = r["plain"]["median_ms"]
+        line["value_no_overlap"] = metric_value(w, r["plain"]["median_ms"] / 1e3, alg, world)[0]
+    if "act_quant" in r:
+        line["act_quant_ms_per_step"] = r["act_quant"]["median_ms"]
     if rank == 0 and not args.no_cpu_baseline:
-        ra = argparse.Namespace(steps=10 ** 6, warmup=1, cpu_seconds=10.0)
+        ra = argparse.Namespace(steps=10 ** 6, warmup=1, cpu_seconds=args.cpu_seconds)
         ref = run_reference(ra, w)
-        line["cpu_baseline"] = {"value": ref["value"], "unit": ref["unit"], "cores": ref["cores"], "kind": "oracle",
-                                "sample": ref["sample"]}
+        line["cpu_baseline"] = {"value": ref["value"] if bound == "hbm" else ref["tflops"], "unit": unit,
+                                "cores": ref["cores"], "kind": "oracle", "sample": ref["sample"]}
+    if per_config:
+        entries = {}
+        for name, m in PER_CONFIG:
+            pw = synth.WORKLOADS[name]
+            if m is not None:
+                pw = dataclasses.replace(pw, M=m)
+            key = name if m is None else f"{name}_m{m}"
+            entries[key] = bench_entry(pw, device, stream, peaks, args.reps, dist, args.decode_max_m or 16,
+                                       0.0 if args.no_cpu_baseline else 3.0, rank)
+            torch.cuda.empty_cache()
+        line["per_config"] = entries
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:

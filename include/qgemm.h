@@ -86,7 +86,9 @@ size_t qgemm_table_bytes(int K, int N, int mode, int block);
 
 /* Bytes of scratch device memory qgemm_run uses for this call (0 if none). The decode path
  * needs it when it splits K across thread blocks (small N); W4A8 needs it for the quantized
- * activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums). The tensor-core
+ * activations (2*M*K bytes of codes as 16-bit values, M scales and M row sums), and with
+ * per-channel weights and K > 8808 also for int32 accumulators [M][N] (4*M*N bytes: the sums are
+ * formed in K-chunks of at most 8192, each exact, and added in int32). The tensor-core
  * path (M above QGEMM_OPT_DECODE_MAX_M) needs 4*M bytes (256-byte aligned) for the row sums of A
  * in INT8 mode with block = K, bf16 activations and M >= 256 (the per-channel scale and offset are
  * then applied in its epilogue), and
@@ -161,8 +163,12 @@ int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float*
 
 /* The W4A8 integer GEMM alone ("S8×S8→S32"): acc[m][n] = sum_k qa[m][k] * q[n][k] with q the
  * 4-bit codes of Bp [N][K/2] read as int8 values 0..15. Writes acc int32 [M][N]. The sums are
- * exact (every partial sum is an integer below 2^24 for K <= 8808). Needs a workspace of
- * qgemm_w4a8_acc_workspace_bytes(M, K) bytes (the codes as 16-bit operands). */
+ * exact for every accepted K: the tensor cores accumulate in float32, which is exact while every
+ * partial sum is an integer below 2^24 (K <= 8808); longer K runs as K-chunks of at most 8192
+ * whose sums are added into acc in int32 (acc is cleared first). K above 1127384, where
+ * 127 * 15 * K could overflow int32, gives QGEMM_ERR_UNSUPPORTED (also for qgemm_run in W4A8
+ * mode). Needs a workspace of qgemm_w4a8_acc_workspace_bytes(M, K) bytes (the codes as 16-bit
+ * operands). */
 int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_t* acc, void* workspace,
                    size_t workspace_bytes, void* stream);
 
@@ -195,6 +201,9 @@ size_t qgemm_w4a8_acc_workspace_bytes(int M, int K);
  *     race on it and may produce wrong results. Order them on one stream. */
 int qgemm_run_noalloc(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
                       const float* T, void* C, int c_dtype, void* stream);
+/* (The array's device address is looked up once per device and kept for the life of the
+ * process. A device reset or a torn-down and recreated primary context invalidates it: reload
+ * the library, or do not call qgemm_run_noalloc again, after cudaDeviceReset.) */
 
 /* ---------------------------------------------------------------- packed-weight files */
 
@@ -245,6 +254,31 @@ int qgemm_load(const char* path, void* Bp, size_t Bp_bytes, float* T, size_t T_b
  * them in a fixed order and rounds once. When 0, it never splits (no workspace needed). The
  * setting is process-wide; it changes qgemm_workspace_bytes for the shapes it affects. */
 #define QGEMM_OPT_SPLIT_K 3
+
+/* QGEMM_OPT_WAIT_LIMIT_US (default 1000000, range 1..1000000). The TMA-fed kernels (the decode
+ * kernel for M <= 16 and the tensor-core kernel) bound every wait of their pipelines by this many
+ * microseconds of the GPU's global timer: a wait that runs out sets the status word that
+ * qgemm_status reports as QGEMM_ERR_TIMEOUT, every role of the thread block leaves its loop, the
+ * copies and MMAs already issued are waited for (always with the full one-second bound) and the
+ * tensor memory is released before the block exits; that call's outputs are then undefined. A
+ * bound shorter than a normal wait makes healthy calls time out: the option exists to exercise
+ * that recovery path, and production code keeps the default. Process-wide. */
+#define QGEMM_OPT_WAIT_LIMIT_US 4
+
+/* QGEMM_OPT_DEBUG_STALL (default 0). Diagnostic: when 1, every following launch of the TMA-fed
+ * kernels has one role (the MMA issuer of the tensor-core kernel, the first consumer warp of the
+ * decode kernel) wait first on a barrier that nothing arrives at, so that the wait runs out after
+ * QGEMM_OPT_WAIT_LIMIT_US and the call ends with QGEMM_ERR_TIMEOUT as described above. It makes
+ * the timeout path testable without a hang; production code keeps 0. Process-wide. */
+#define QGEMM_OPT_DEBUG_STALL 5
+
+/* QGEMM_OPT_FAULT_INJECT (default 0, or the value of the environment variable QGEMM_FAULT_INJECT
+ * when the library loads). Host-side fault injection: when n > 0, the n-th compute call from now
+ * (qgemm_pack, qgemm_run, qgemm_run_fused, qgemm_run_noalloc, qgemm_act_quant, qgemm_w4a8_acc)
+ * passes its argument checks and then returns QGEMM_ERR_CUDA with the detail "simulated launch
+ * failure" instead of launching, as a failed launch would; the count then stays 0. No GPU fault is
+ * involved. For testing callers' error handling. Process-wide. */
+#define QGEMM_OPT_FAULT_INJECT 6
 
 /* Set an option; returns its previous value, or QGEMM_ERR_ARG for an unknown option or value. */
 int qgemm_set_option(int option, int value);

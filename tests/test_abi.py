@@ -41,6 +41,13 @@ def test_sizes():
     # W4A8: qa (M*K bytes), scales and row sums, each 256-byte aligned
     assert qg.qgemm_workspace_bytes(2048, 4096, 14336, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == 2 * 2048 * 4096 + 2 * 8192
     assert qg.qgemm_w4a8_acc_workspace_bytes(2048, 4096) == 2 * 2048 * 4096
+    # W4A8, per-channel weights and K past 8808 (one float32 accumulation no longer exact): the
+    # K-chunks' int32 accumulators [M][N] follow
+    assert qg.qgemm_workspace_bytes(16, 8832, 40, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == (
+        2 * 16 * 8832 + 2 * 256 + (-(-16 * 40 * 4 // 256)) * 256)
+    assert qg.qgemm_workspace_bytes(16, 8768, 40, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == 2 * 16 * 8768 + 2 * 256
+    # block-quantized W4A8 weights multiply float weights: no int32 chunks
+    assert qg.qgemm_workspace_bytes(16, 8832, 40, qg.MODE_W4A8, 64, qg.BF16, qg.BF16) == 2 * 16 * 8832 + 2 * 256
     # decode with a large N needs no scratch; a small N splits K across blocks
     assert qg.qgemm_workspace_bytes(1, 4096, 11008, qg.MODE_INT4, 64, qg.BF16, qg.BF16) == 0
     assert qg.qgemm_workspace_bytes(1, 4096, 512, qg.MODE_INT4, 64, qg.BF16, qg.BF16) > 0
@@ -94,6 +101,11 @@ def test_pack_and_aux_reject():
     assert lib.qgemm_act_quant(4, 128, FAKE, 2, FAKE + 2, FAKE, FAKE, None) == -3
     assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, None, FAKE, FAKE, 1 << 20, None) == -1
     assert lib.qgemm_w4a8_acc(4, 128, 8, FAKE, FAKE, FAKE, FAKE, 16, None) == -4      # workspace too small
+    # K whose int32 accumulators could overflow (127 * 15 * K > 2^31 - 1)
+    big_k = (2147483647 // (127 * 15) // 64 + 1) * 64
+    assert lib.qgemm_w4a8_acc(4, big_k, 8, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == -2
+    assert lib.qgemm_w4a8_acc(4, big_k - 64, 8, FAKE, None, FAKE, FAKE, 1 << 40, None) == -1   # passes the K check
+    assert lib.qgemm_run(4, big_k, 8, 3, 0, FAKE, 2, FAKE, FAKE, FAKE, 2, FAKE, 1 << 40, None) == -2
 
 
 def test_options():
@@ -171,3 +183,60 @@ def test_tensor_core_split_rule(M, K, N):
         else:
             want = min(152 // tiles, (K // 64) // 8)
             assert want < (3 if bn >= 256 else 2)
+
+
+def test_fault_injection_simulates_a_launch_failure():
+    """QGEMM_OPT_FAULT_INJECT: the n-th compute call reports QGEMM_ERR_CUDA without launching;
+    rejected calls do not count. Each case sets n = 1, so no call here reaches a launch."""
+    lib = qg.load()
+    assert qg.qgemm_get_option(qg.OPT_FAULT_INJECT) == 0
+    run = lambda M, K: lib.qgemm_run(M, K, 11008, 1, 64, FAKE, 2, FAKE, FAKE, FAKE, 2, FAKE, 0, None)
+    try:
+        assert qg.qgemm_set_option(qg.OPT_FAULT_INJECT, 1) == 0
+        assert run(1, 100) == -2                           # rejected first: not counted
+        assert qg.qgemm_get_option(qg.OPT_FAULT_INJECT) == 1
+        assert run(1, 4096) == -5
+        assert "simulated launch failure" in qg.qgemm_last_error()
+        assert qg.qgemm_get_option(qg.OPT_FAULT_INJECT) == 0
+        assert run(0, 4096) == 0                           # empty calls launch nothing and are not counted
+        cases = [
+            lambda: lib.qgemm_pack(FAKE, 4096, 64, 1, 64, 0, FAKE, FAKE, None),
+            lambda: lib.qgemm_act_quant(4, 128, FAKE, 2, FAKE, FAKE, FAKE, None),
+            lambda: lib.qgemm_w4a8_acc(4, 128, 8, FAKE, FAKE, FAKE, FAKE, 1 << 20, None),
+            lambda: lib.qgemm_run_fused(4, 128, 8, 1, 64, FAKE, 2, FAKE, FAKE, None, 2, None, FAKE, 2, None, 0, None),
+        ]
+        for call in cases:
+            qg.qgemm_set_option(qg.OPT_FAULT_INJECT, 1)
+            assert call() == -5
+            assert "simulated launch failure" in qg.qgemm_last_error()
+        qg.qgemm_set_option(qg.OPT_FAULT_INJECT, 1)
+        with pytest.raises(qg.QgemmError) as ei:          # the binding raises it like any failure
+            qg.qgemm_run(1, 4096, 11008, 1, 64, FAKE, 2, FAKE, FAKE, FAKE, 2, FAKE, 0, stream=0)
+        assert ei.value.code == -5
+        assert lib.qgemm_set_option(qg.OPT_FAULT_INJECT, -1) == -1
+    finally:
+        qg.qgemm_set_option(qg.OPT_FAULT_INJECT, 0)
+
+
+def test_fault_injection_from_environment():
+    code = ("import weight_quantized_gemm_gb300 as qg; "
+            "print(qg.qgemm_get_option(qg.OPT_FAULT_INJECT))")
+    import os
+    import sys
+    env = dict(os.environ, QGEMM_FAULT_INJECT="3")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=root)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "3"
+
+
+def test_wait_limit_and_stall_options():
+    assert qg.qgemm_get_option(qg.OPT_WAIT_LIMIT_US) == 1000000
+    assert qg.qgemm_set_option(qg.OPT_WAIT_LIMIT_US, 500) == 1000000
+    assert qg.qgemm_set_option(qg.OPT_WAIT_LIMIT_US, 1000000) == 500
+    assert qg.load().qgemm_set_option(qg.OPT_WAIT_LIMIT_US, 0) == -1
+    assert qg.load().qgemm_set_option(qg.OPT_WAIT_LIMIT_US, 1000001) == -1
+    assert qg.qgemm_get_option(qg.OPT_DEBUG_STALL) == 0
+    assert qg.qgemm_set_option(qg.OPT_DEBUG_STALL, 1) == 0
+    assert qg.qgemm_set_option(qg.OPT_DEBUG_STALL, 0) == 1
+    assert qg.load().qgemm_set_option(qg.OPT_DEBUG_STALL, 2) == -1

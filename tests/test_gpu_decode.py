@@ -159,11 +159,21 @@ def test_act_quant_bit_exact(a_dtype):
     M, K = 2048, 4096
     w = synth.Workload("t", M, K, 1, 3, 0, a_dtype, 2, 0, 0)
     A_np = synth.make_activations(w)
-    A32 = oracle.values(A_np, a_dtype).astype(np.float32)
-    A32_rows = A32.copy()
     A_np = A_np.copy()
     A_np[17] = 0                                           # a zero row: scale 0, codes 0
-    A32_rows[17] = 0
+    # rows of tiny values (with zeros among them) whose scale max|a| / 127 is a subnormal float32,
+    # where a reciprocal of the scale overflows; f16 cannot hold such values, so its tiny rows
+    # sit at the bottom of its own range instead
+    base = oracle.values(A_np[40], a_dtype)
+    tiny_rows = ((33, 1e-38), (34, 2e-40)) if a_dtype != synth.F16 else ((33, 1e-6), (34, 2e-7))
+    for row, tiny in tiny_rows:
+        x = base * tiny
+        x[::5] = 0.0
+        A_np[row] = synth.encode(x, a_dtype)
+    A32_rows = oracle.values(A_np, a_dtype).astype(np.float32)
+    assert A32_rows[33].any() and A32_rows[34].any()
+    if a_dtype != synth.F16:
+        assert np.abs(A32_rows[33]).max() / np.float32(127) < np.finfo(np.float32).tiny
     qa_r, s_r, rs_r = oracle.act_quant(A32_rows)
     A = torch_from(A_np, a_dtype)
     qa = torch.empty((M, K), dtype=torch.int8, device=DEV)

@@ -152,6 +152,42 @@ def test_w4a8_acc_extreme_codes_exact():
     assert np.array_equal(acc, oracle.w4a8_acc(qa, q))
 
 
+@pytest.mark.parametrize("K,N", [(8832, 40), (16448, 40), (8832, 42)])
+def test_w4a8_acc_extreme_codes_long_k_exact(K, N):
+    """K past 8808: the extreme sums 127 * 15 * K exceed 2^24, so one float32 accumulation would
+    round them; the library runs K-chunks that are each exact and adds them in int32 (N = 42:
+    rows that are no whole number of 16-byte units, added element by element)."""
+    M = 5
+    qa = np.full((M, K), 127, dtype=np.int8)
+    qa[1] = -127
+    qa[2, ::2] = -127
+    qa[3] = np.where(np.arange(K) % 3 == 0, 127, -1).astype(np.int8)
+    qa[4] = np.where(np.arange(K) % 7 == 0, -127, 126).astype(np.int8)
+    W = np.ones((K, N), dtype=np.float32)
+    W[0, :] = -1.0                               # codes: 0 at k = 0, 15 elsewhere
+    W[1, ::3] = -1.0
+    q, _ = oracle.quantize(W, K, 15)
+    Bp, _ = gpu_pack(W, 3, 0)
+    ref = oracle.w4a8_acc(qa, q)
+    assert np.abs(ref).max() > 2 ** 24
+    acc = _gpu_w4a8_acc(qa, Bp, M, K, N)
+    assert np.array_equal(acc, ref)
+    acc = _gpu_w4a8_acc(qa, Bp, M, K, N)         # twice: the chunks add into a cleared array
+    assert np.array_equal(acc, ref)
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 8832, 40), (130, 8832, 136)])
+@pytest.mark.parametrize("a_dtype", [synth.BF16, synth.F32])
+def test_w4a8_layer_long_k(M, K, N, a_dtype):
+    """The W4A8 layer with K past the exact range of one float32 accumulation (int32 K-chunks,
+    then the rescale): against the oracle's integer path."""
+    w, A_np, W_np = _w4a8_inputs(M, K, N, a_dtype)
+    ref = oracle.reference_layer(3, 0, A_np, a_dtype, W_np)
+    Bp, T = gpu_pack(W_np, 3, 0)
+    got = gpu_run(M, K, N, 3, 0, A_np, a_dtype, Bp, T, synth.BF16)
+    check_close(got, ref["R"], a_dtype if a_dtype != synth.F32 else synth.BF16, synth.BF16, "w4a8 long K")
+
+
 @pytest.mark.parametrize("M,K,N", [(1, 128, 40), (33, 512, 100), (300, 1024, 257)])
 @pytest.mark.parametrize("a_dtype", [synth.BF16, synth.F16, synth.F32])
 def test_w4a8_layer(M, K, N, a_dtype):
@@ -175,11 +211,14 @@ def test_w4a8_m2048_k4096_n14336_sampled():
     mi, ni = rng.integers(0, w.M, 4096), rng.integers(0, w.N, 4096)
     acc_ref = oracle.w4a8_acc_points(qa, q, mi, ni)
     assert np.array_equal(acc[mi, ni], acc_ref)
-    # the layer: within the bar at the same points (expected values from the oracle alone)
+    # the layer: every output of 24 sampled rows, expected values from the oracle's own integer
+    # GEMM and rescale
     got = gpu_run(w.M, w.K, w.N, 3, 0, A_np, w.a_dtype, Bp, Tg, w.c_dtype)
-    R = (s[mi].astype(np.float64) * (T[ni, 0, 1].astype(np.float64) * acc_ref.astype(np.float64) +
-                                      T[ni, 0, 0].astype(np.float64) * rs[mi]))
-    check_close(got[mi, ni], R, w.a_dtype, w.c_dtype, w.name)
+    rows = np.sort(rng.choice(w.M, 24, replace=False))
+    acc_rows = oracle.w4a8_acc(qa[rows], q)
+    assert np.array_equal(acc[rows], acc_rows)
+    R = oracle.w4a8_out(acc_rows, s[rows], rs[rows], T)
+    check_close(got[rows], R, w.a_dtype, w.c_dtype, w.name)
 
 
 @pytest.mark.parametrize("M,K,N,block", [(1, 256, 40, 64), (40, 512, 96, 64), (300, 1024, 130, 128), (64, 2048, 256, 64)])

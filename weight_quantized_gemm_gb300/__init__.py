@@ -15,7 +15,7 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "qgemm_run_fused", "qgemm_save", "qgemm_load_info", "qgemm_load", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "OPT_WAIT_LIMIT_US", "OPT_DEBUG_STALL", "OPT_FAULT_INJECT", "qgemm_run_fused", "qgemm_save", "qgemm_load_info", "qgemm_load", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
@@ -23,6 +23,9 @@ MODE_FLOAT, MODE_INT4, MODE_INT8, MODE_W4A8 = 0, 1, 2, 3
 OPT_LAUNCH_OVERLAP = 1
 OPT_DECODE_MAX_M = 2
 OPT_SPLIT_K = 3
+OPT_WAIT_LIMIT_US = 4
+OPT_DEBUG_STALL = 5
+OPT_FAULT_INJECT = 6
 ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH = 0, 1, 2, 3
 NOALLOC_SCRATCH_BYTES = 4 << 20
 F32, F16, BF16 = 0, 1, 2

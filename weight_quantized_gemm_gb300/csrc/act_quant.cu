@@ -6,7 +6,10 @@
 // the correctly rounded IEEE quotient bit for bit. The quotient itself is not needed, only the
 // integer it rounds to, so each element first uses y = a * RN(1 / as): for |a / as| <= 127 it is
 // within 2.3e-5 of RN(a / as), hence rounds to the same integer unless it lies within 3e-5 of a
-// half-integer; only those rare elements take the exact division.
+// half-integer; only those rare elements take the exact division. A row whose scale is below the
+// smallest normal float32 (max|a| < 127 * 2^-126) takes the exact division for every element:
+// RN(1 / as) can overflow there (to +inf below 2^-128), and the error bound above assumes a
+// normal reciprocal.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,9 +44,11 @@ __device__ __forceinline__ void load8(const void* A, size_t i, float (&v)[8]) {
 }
 
 // The codes of 8 values: RN-even of v * RN(1/s) unless one of them lies within 3e-5 of a
-// half-integer, then of the correctly rounded quotient for all 8; clamped to +-127 (as rounded
-// floats, exact); the f16 copies, the int8 bytes and the running sum of the codes.
-__device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rcp, int& sum, uint4& h16, uint2& q8) {
+// half-integer (or the row's scale is subnormal: `exact`), then of the correctly rounded quotient
+// for all 8; clamped to +-127 (as rounded floats, exact); the f16 copies, the int8 bytes and the
+// running sum of the codes.
+__device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rcp, bool exact, int& sum, uint4& h16,
+                                          uint2& q8) {
     float r[8];
     float dev = 0.f;
 #pragma unroll
@@ -52,7 +57,7 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rc
         r[j] = rintf(y);
         dev = fmaxf(dev, fabsf(y - r[j]));   // distance to the nearest integer, <= 0.5
     }
-    if (dev > 0.49997f) {   // near a half-integer: decide by the exact quotient
+    if (exact || dev > 0.49997f) {   // near a half-integer: decide by the exact quotient
 #pragma unroll
         for (int j = 0; j < 8; ++j) r[j] = rintf(__fdiv_rn(v[j], s));
     }
@@ -114,13 +119,15 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, s_max[w]);
     const float s = __fdiv_rn(amax, 127.0f);
-    const float rcp = s != 0.f ? __frcp_rn(s) : 0.f;   // s == 0: every code is 0
+    // s == 0: every code is 0. A subnormal s (its reciprocal may overflow) divides exactly.
+    const bool exact = s != 0.f && s < 1.17549435e-38f;
+    const float rcp = (s != 0.f && !exact) ? __frcp_rn(s) : 0.f;
 
     int sum = 0;
     auto emit = [&](int k, const float (&w)[8]) {
         uint4 h16;
         uint2 q8;
-        quantize8(w, s, rcp, sum, h16, q8);
+        quantize8(w, s, rcp, exact, sum, h16, q8);
         if (qa16) *reinterpret_cast<uint4*>(qa16 + row + k) = h16;
         if (qa) *reinterpret_cast<uint2*>(qa + row + k) = q8;
     };

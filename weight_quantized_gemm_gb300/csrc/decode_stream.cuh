@@ -67,7 +67,7 @@ struct Budget {
     static constexpr int kRedBytes = kRed * kCWarps * NT * 32 * 16;       // a float4 per lane, tile, warp, unit
     static constexpr int kFragBytes = NT == 1 ? 0 : kCWarps * kNJ * NT * 1024;
     static constexpr int kSumBytes = NT == 1 ? 0 : kCWarps * kNJ * NT * 32;
-    static constexpr int kFixedBytes = kRedBytes + kCWarps * NT * 32 + kFragBytes + kSumBytes + 2 * kMaxDepth * 8 + 16;
+    static constexpr int kFixedBytes = kRedBytes + kCWarps * NT * 32 + kFragBytes + kSumBytes + (2 * kMaxDepth + 1) * 8 + 16;
 };
 
 template <int FMT>
@@ -96,6 +96,8 @@ struct Params {
     unsigned int* status;
     Epilogue ep;        // applied to the final sums (not to split partials) by the EP kernels
     int cdt;            // C's type
+    long long wait_ns;  // bound of each pipeline wait (the producer's drain: ptx::kWaitNs)
+    int stall;          // diagnostic: consumer warp 0 first waits on a barrier nothing arrives at
 };
 
 __device__ __forceinline__ float2 lds64f(uint32_t addr) {
@@ -134,17 +136,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     float* wsum = red + Bu::kRedBytes / 4;                                            // [warp][tile][8] column sums
     uint8_t* fragp = reinterpret_cast<uint8_t*>(wsum + kCWarps * NT * 8);   // [warp][jj][tile][plane][lane] 16 B
     float2* fsum = reinterpret_cast<float2*>(fragp + Bu::kFragBytes);       // [warp][jj][tile][t] column sums
-    uint64_t* bars = reinterpret_cast<uint64_t*>(fragp + Bu::kFragBytes + Bu::kSumBytes);   // full | empty
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxDepth);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(fragp + Bu::kFragBytes + Bu::kSumBytes);   // full | empty | stall
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kMaxDepth + 1);
     const uint32_t s_base = smem_u32(smem);
     auto full = [&](int s) { return smem_u32(bars + s); };
     auto empty = [&](int s) { return smem_u32(bars + kMaxDepth + s); };
+    const uint32_t stall_bar = smem_u32(bars + 2 * kMaxDepth);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.depth; ++s) {
             ptx::mbar_init(full(s), 1);   // the producer's expect_tx arrival
             ptx::mbar_init(empty(s), kCWarps);
         }
+        ptx::mbar_init(stall_bar, 1);
         // the swizzled TMA boxes need 1024-byte aligned stages
         *abort_flag = (s_base & 1023u) != 0;
         if (*abort_flag) atomicOr(p.status, kStatusMisaligned);
@@ -169,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             const int n0 = (int)blockIdx.x * kRows + ui * n_step;
             for (int c = 0; c < chunks; ++c) {
                 bool got = true;
-                if (lane == 0) got = ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, p.status);
+                // no stage is issued after an abort (consumers then stop releasing slots)
+                if (lane == 0) got = !*abort_flag && ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, p.status, p.wait_ns);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                     ok = false;
                     break;
@@ -297,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    if (p.stall && warp == 0)   // diagnostic: runs out and raises the abort flag
+        ok = ptx::mbar_wait(stall_bar, 0u, abort_flag, p.status, p.wait_ns);
     for (int ui0 = 0; ui0 < nu; ui0 += kRed) {
         const int nr = min(kRed, nu - ui0);
         for (int r = 0; r < nr; ++r) {
@@ -309,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 if (c >= chunks) break;
-                ok = ok && ptx::mbar_wait(full(s), ph, abort_flag, p.status);
+                ok = ok && ptx::mbar_wait(full(s), ph, abort_flag, p.status, p.wait_ns);
                 // the stage holds slices [0, sl_end - first slice): a warp past them has nothing
                 // loaded (stale bytes could even read as non-finite 16-bit weights)
                 if (ok && warp < sl_end - (sl_begin + c * p.bz)) {
@@ -401,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
                     }
                 }
                 __syncwarp();   // every lane has read the stage
-                if (lane == 0) ptx::mbar_arrive(empty(s));
+                // A slot is released only once its copy has landed (lane 0 saw it complete): after an
+                // abort no slot whose copy may still be in flight is handed back to the producer.
+                if (lane == 0 && ok) ptx::mbar_arrive(empty(s));
                 if (++s == p.depth) {
                     s = 0;
                     ph ^= 1u;
@@ -539,6 +548,8 @@ cudaError_t launch_v(const DecodeArgs& a, cudaStream_t s) {
     plan.p.cdt = a.c_dtype;
     plan.p.status = status_word_address();
     if (!plan.p.status) return cudaErrorInvalidValue;
+    plan.p.wait_ns = option_wait_ns();
+    plan.p.stall = option_stall();
     CUtensorMap wmap;
     cudaError_t e = make_wmap(&wmap, a.Bp, plan.p.row_bytes, a.N, plan.p.bz);
     if (e != cudaSuccess) return e;

@@ -114,11 +114,26 @@ struct W4A8Args {
     int c_dtype;
     Epilogue ep;    // applied to the rescaled output
     int block = 0;  // K-block of the weights' {offset, scale} (0 or K: per channel)
+    int splits = 1; // K-chunks (grid z); with acc_add each chunk adds its int32 sums into acc
+    int acc_add = 0;
 };
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
+// The integer sums of the W4A8 tensor-core GEMM are exact while every float32 partial sum is an
+// integer below 2^24: |qa| <= 127 and q <= 15 bound a K-chunk's sum by 1905 * chunk, so chunks of
+// at most 8808 (8192 used, a multiple of 64) stay exact. Longer K runs as K-chunks whose int32
+// sums are added in int32 (exact, in any order).
+constexpr int kW4A8ExactK = 8808;
+constexpr int kW4A8ChunkK = 8192;
+inline int w4a8_exact_splits(int K) { return K <= kW4A8ExactK ? 1 : (K + kW4A8ChunkK - 1) / kW4A8ChunkK; }
+// C = epilogue(as[m] * (ws[n] * acc[m][n] + off[n] * rowsum[m])) from int32 accumulators (W4A8 with
+// per-channel weights when K was split into exact chunks); T is the grouped table (one block).
+cudaError_t launch_w4a8_rescale(int M, int N, const int32_t* acc, const float* as, const int32_t* rowsum,
+                                const float* T, const Epilogue& ep, void* C, int c_dtype, cudaStream_t s);
 
 // library options (qgemm_set_option)
 int option_overlap();
+long long option_wait_ns();   // bound of each pipeline wait in the TMA-fed kernels
+int option_stall();           // diagnostic stall of the next launches (QGEMM_OPT_DEBUG_STALL)
 // Records `detail` as the thread's last error and returns `code` (the C ABI's error path).
 int api_fail(int code, const char* detail);
 // Bp bytes of a shape (0 if the shape is invalid) and, in *table_bytes, its T bytes (0 in FLOAT).

@@ -12,7 +12,36 @@ __global__ void codes_to_f16_kernel(const int8_t* __restrict__ qa, __half* __res
         out[i] = __int2half_rn(qa[i]);
 }
 
+// C = epilogue(as * (ws * acc + off * rowsum)) with the same float32 steps as the tensor-core
+// kernel's W4A8 epilogue: fma(ws, as * acc, off * (as * rowsum)).
+template <int CDT>
+__global__ void w4a8_rescale_kernel(int M, int N, const int32_t* __restrict__ acc, const float* __restrict__ as,
+                                    const int32_t* __restrict__ rowsum, const float* __restrict__ T, Epilogue ep,
+                                    void* C) {
+    const size_t count = (size_t)M * N;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < count; i += (size_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i / (size_t)N), n = (int)(i - (size_t)m * N);
+        const float a = __ldg(as + m);
+        const float2 t = __ldg(reinterpret_cast<const float2*>(T + tab_index(n, 1, 0) * 2));   // {off, ws}
+        const float y = fmaf(t.y, a * (float)__ldg(acc + i), t.x * (a * (float)__ldg(rowsum + m)));
+        store_c<CDT>(C, i, epilogue_apply<CDT>(ep, y, i, n));
+    }
+}
+
 }  // namespace pf
+
+cudaError_t launch_w4a8_rescale(int M, int N, const int32_t* acc, const float* as, const int32_t* rowsum,
+                                const float* T, const Epilogue& ep, void* C, int c_dtype, cudaStream_t s) {
+    const int threads = 256;
+    const size_t want = ((size_t)M * N + threads - 1) / threads;
+    const int blocks = (int)(want < 8192 ? want : 8192);
+    switch (c_dtype) {
+        case DT_F32: pf::w4a8_rescale_kernel<DT_F32><<<blocks, threads, 0, s>>>(M, N, acc, as, rowsum, T, ep, C); break;
+        case DT_F16: pf::w4a8_rescale_kernel<DT_F16><<<blocks, threads, 0, s>>>(M, N, acc, as, rowsum, T, ep, C); break;
+        default: pf::w4a8_rescale_kernel<DT_BF16><<<blocks, threads, 0, s>>>(M, N, acc, as, rowsum, T, ep, C); break;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prefill_codes8(const pf::Maps& maps, const pf::Params& p, int kdt, cudaStream_t s) {
     return pf::launch_wf<pf::WF_CODES8, true, pf::EPI_W4A8>(maps, p, kdt, s);
@@ -24,9 +53,14 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.M = a.M; p.K = a.K; p.N = a.N; p.block = block; p.nb = a.K / block;
     p.BN = pf::pick_bn(a.M);
     p.Bp = static_cast<const uint8_t*>(a.Bp); p.T = a.T; p.C = a.C;
-    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc; p.splits = 1;
+    p.a_scale = a.as; p.rowsum = a.rowsum; p.acc = a.acc;
+    p.splits = a.splits > 1 ? a.splits : 1;
+    p.acc_add = a.acc_add;
+    if (p.splits > 1 && !(a.acc && a.acc_add)) return cudaErrorInvalidValue;   // K-chunks add int32 sums
     p.status = status_word_address();
     if (!p.status) return cudaErrorInvalidValue;
+    p.wait_ns = option_wait_ns();
+    p.stall = option_stall();
     p.ep = a.acc ? Epilogue{} : a.ep;
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);

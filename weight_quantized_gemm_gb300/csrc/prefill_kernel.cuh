@@ -20,9 +20,10 @@
 // writes float32 partial sums and a second kernel adds them in a fixed order.
 // W4A8 ("W4 解包为 INT8 ... S8×S8→S32", «测试用例与注册机制») uses the same kernel with the 4-bit
 // codes as exact f16 integers and the activation codes as exact f16 integers: every product is
-// an integer below 2^11 and every partial sum an integer below 2^24, so the float32 tensor-core
-// accumulation is exact and equals the int32 sum; the epilogue then either stores it as int32
-// or applies as * (ws * acc + off * rowsum).
+// an integer below 2^11 and, over at most 8808 of K, every partial sum an integer below 2^24, so
+// the float32 tensor-core accumulation is exact and equals the int32 sum; the epilogue then
+// either stores it as int32 (or adds it into int32 accumulators, one K-chunk per split, for
+// longer K) or applies as * (ws * acc + off * rowsum).
 // Int8-Block0 (one {offset, scale} per channel, «为什么用 Conv1x1 来测 GEMM») takes the same route
 // with float activations: sum_k a (q s + o) = s * sum_k a q + o * sum_k a, so the MMA multiplies
 // the raw 8-bit codes (exact 16-bit integers, also in bf16: no hi/lo weight split) and the
@@ -69,12 +70,16 @@ struct Params {
     const int32_t* rowsum;    // W4A8: per-row sum of activation codes
     const float* rowsum_f;    // CODES8: per-row float32 sum of the activations (when rowsum is null)
     int32_t* acc;             // EPI_ACC output
+    int acc_add;              // EPI_ACC: add the tile into acc (int32, exact) instead of storing it; the
+                              // K-splits then all add into the one [M][N] array
     int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
     int r_tma;                // the epilogue's residual tile comes in by one TMA load (Maps::r)
     int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
     int tblocks;              // K-blocks per table box (min(SUB, nb))
     unsigned int* status;     // the library's device status word (bounded waits that gave up)
     Epilogue ep;              // bias / activation / residual (none when the output is split partials)
+    long long wait_ns;        // bound of each pipeline wait (waits that drain issued work: ptx::kWaitNs)
+    int stall;                // diagnostic: the MMA issuer first waits on a barrier nothing arrives at
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -363,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr int kRowB = WBox<WF>::kRowBytes;
     constexpr int kLo = SUB * 32;                      // TMEM column of the low parts in an A stage (Split)
     extern __shared__ __align__(1024) uint8_t smem[];
-    // bounded mbarrier wait reporting to the library's status word
+    // bounded pipeline wait reporting to the library's status word
     auto mbar_wait = [&](uint32_t bar, uint32_t parity, volatile int* abort) {
-        return ptx::mbar_wait(bar, parity, abort, p.status);
+        return ptx::mbar_wait(bar, parity, abort, p.status, p.wait_ns);
     };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t kABytes = (uint32_t)BN * kBK * 2;   // one activation box
@@ -381,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
     // bars: full[S] (the stage's boxes landed) | full_a[S] (TMEM A stage written) |
     //       empty[S] (MMAs of the stage done) | acc_full
-    // ... | res_full (the residual tile landed, Params::r_tma)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 2);
+    // ... | res_full (the residual tile landed, Params::r_tma) | stall (Params::stall: never arrived at)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
     float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
@@ -392,6 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     auto empty = [&](int s) { return smem_u32(bars + 2 * kMaxStages + s); };
     const uint32_t acc_full = smem_u32(bars + 3 * kMaxStages);
     const uint32_t res_full = smem_u32(bars + 3 * kMaxStages + 1);
+    const uint32_t stall_bar = smem_u32(bars + 3 * kMaxStages + 2);
+    static_assert((3 * kMaxStages + 3) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
     // bytes of the staged output tile [BN rows][128 channels], where the residual tile also lands
     constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
     static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
@@ -404,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         mbar_init(acc_full, 1);
         mbar_init(res_full, 1);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
@@ -429,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             uint32_t ph = 0;
             for (int i = 0; i < nks; ++i) {
                 const int ks = ks0 + i;
-                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+                if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
                 const uint32_t st = st_s + (uint32_t)s * SB;
                 mbar_expect_tx(full_x(s), bytes);
 #pragma unroll
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (*abort_flag) {   // let the copies already issued land before the block exits
                 for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
                     volatile int never = 0;
-                    mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never);
+                    ptx::mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never, p.status);
                 }
             } else if (EPI != EPI_ACC && p.r_tma) {
                 // The residual tile lands where the output tile is staged, [0, kTileBytes): as
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     mbar_expect_tx(res_full, kTileBytes);
                     ptx::tma_load_3d(st_s, &maps.r, n_tile, m_tile, 0, res_full);
                     volatile int never = 0;   // stay until it has landed (the epilogue reads it)
-                    mbar_wait(res_full, 0u, &never);
+                    ptx::mbar_wait(res_full, 0u, &never, p.status);
                 }
             }
         }
@@ -473,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint32_t idesc = idesc_f16(BF, BN, kBM);
             int s = 0;
             uint32_t ph = 0;
+            if (p.stall) mbar_wait(stall_bar, 0u, abort_flag);   // diagnostic: runs out, raises the abort flag
             for (int i = 0; i < nks; ++i) {
                 // With dequant warps, full_a is enough: every dequant warp waited for the stage's
                 // TMA barrier (activations included) before it arrived on full_a, so acquiring
@@ -664,7 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             ptx::fence_proxy_async_smem();
             asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
             if (ok && threadIdx.x == 64) {
-                ptx::tma_store_3d(&maps.c, n_tile, m_tile, blockIdx.z, smem_u32(tile));
+                if (EPI == EPI_ACC && p.acc_add)
+                    ptx::tma_reduce_add_3d(&maps.c, n_tile, m_tile, 0, smem_u32(tile));
+                else
+                    ptx::tma_store_3d(&maps.c, n_tile, m_tile, blockIdx.z, smem_u32(tile));
                 ptx::bulk_commit();
                 ptx::bulk_wait_read();
             }
@@ -674,8 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
             constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
             constexpr int kChunks = kBM / kPer;               // chunks per tile row
+            const bool add = EPI == EPI_ACC && p.acc_add;
             uint8_t* out = (EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C)) +
-                           (size_t)blockIdx.z * p.M * p.N * kEsz;
+                           (add ? 0 : (size_t)blockIdx.z * p.M * p.N * kEsz);
             const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
             for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
                 const int ml = idx / kChunks, c = idx - ml * kChunks;
@@ -683,7 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (n0 >= nvalid) continue;
                 const uint8_t* src = tile + ((size_t)ml * kBM + n0) * kEsz;
                 uint8_t* dst = out + ((size_t)(m_tile + ml) * p.N + n_tile + n0) * kEsz;
-                if (vec && n0 + kPer <= nvalid) {
+                if (add) {   // int32 accumulators of one K-chunk added in (exact, any order)
+                    for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
+                        atomicAdd(reinterpret_cast<int*>(dst) + e, reinterpret_cast<const int*>(src)[e]);
+                } else if (vec && n0 + kPer <= nvalid) {
                     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
                 } else {
                     for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
@@ -696,6 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        if (*abort_flag) {
+            // After an abort the epilogue may not have waited for acc_full: the MMAs already issued
+            // finish before their tensor memory is released (acc_full is committed on every path).
+            volatile int never = 0;
+            ptx::mbar_wait(acc_full, 0u, &never, p.status);
+        }
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

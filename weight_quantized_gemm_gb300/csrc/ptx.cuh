@@ -8,10 +8,18 @@
 namespace qg {
 namespace ptx {
 
-// A bounded wait gives up after about one second at GB300 clocks.
-constexpr long long kWaitCycles = 2000000000LL;
+// A bounded wait gives up after this many nanoseconds of the GPU's global timer (one second)
+// unless the launch passes a shorter bound; waits that drain copies or MMAs already issued always
+// take this one.
+constexpr long long kWaitNs = 1000000000LL;
 // Bit set in the library's device status word by a wait that gave up.
 constexpr unsigned kStatusTimeout = 1u;
+
+__device__ __forceinline__ long long global_ns() {
+    long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -37,18 +45,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase of `parity` to complete. Gives up after kWaitCycles or as soon as another
-// role has raised the block's abort flag; a wait that runs out raises the flag itself and sets
-// kStatusTimeout in *status. Returns false if it gave up.
+// Waits for the phase of `parity` to complete. Gives up after limit_ns nanoseconds or as soon as
+// another role has raised the block's abort flag; a wait that runs out raises the flag itself and
+// sets kStatusTimeout in *status. Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* status) {
+                                          unsigned int* status, long long limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
+    const long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
@@ -82,6 +90,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
 // Tiled 3-D TMA store of one box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+// Tiled 3-D TMA reduce-add of one box from shared memory into global memory (element type from
+// the tensor map; for int32 the adds are exact and their order does not matter).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");

@@ -2,6 +2,7 @@
 // Every check runs before the first launch, so a rejected call enqueues nothing.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <atomic>
 #include <mutex>
@@ -15,6 +16,25 @@ thread_local char g_last_error[256] = "";
 std::atomic<int> g_opt_overlap{0};
 std::atomic<int> g_opt_decode_max_m{16};
 std::atomic<int> g_opt_split_k{1};
+std::atomic<int> g_opt_wait_us{1000000};
+std::atomic<int> g_opt_stall{0};
+
+// QGEMM_OPT_FAULT_INJECT: the n-th compute call from now reports a simulated launch failure.
+int fault_from_env() {
+    const char* v = getenv("QGEMM_FAULT_INJECT");
+    if (!v || !*v) return 0;
+    const long n = strtol(v, nullptr, 10);
+    return n > 0 && n < 1000000000L ? (int)n : 0;
+}
+std::atomic<int> g_fault{fault_from_env()};
+
+// Counts one compute call down; true for the call the countdown selected.
+bool inject_fault() {
+    int v = g_fault.load();
+    while (v > 0)
+        if (g_fault.compare_exchange_weak(v, v - 1)) return v == 1;
+    return false;
+}
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -54,9 +74,17 @@ size_t packed_bytes(int K, int N, int mode, int w_dtype) {
 }
 
 // W4A8 workspace: the activation codes as f16 [M][K] (exact integers, the tensor cores' operand
-// type), then as [M] f32 and rowsum [M] int32, each 256-byte aligned.
+// type), then as [M] f32 and rowsum [M] int32, each 256-byte aligned; with per-channel weights and
+// K beyond the exact range of one float32 accumulation (qg::w4a8_exact_splits), then the int32
+// accumulators [M][N] that the K-chunks add into.
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-size_t w4a8_ws(int M, int K) { return align256((size_t)M * K * 2) + align256((size_t)M * 4) * 2; }
+bool w4a8_chunked(int K, int block) { return block == K && qg::w4a8_exact_splits(K) > 1; }
+size_t w4a8_ws(int M, int K, int N, int block) {
+    return align256((size_t)M * K * 2) + align256((size_t)M * 4) * 2 +
+           (w4a8_chunked(K, block) ? align256((size_t)M * N * 4) : 0);
+}
+// Largest K whose int32 accumulators cannot overflow: |qa| * q <= 127 * 15 per term.
+constexpr int kW4A8MaxK = 2147483647 / (127 * 15);
 
 int fmt_of(int mode) {
     return mode == QGEMM_MODE_FLOAT ? qg::FMT_FLOAT : (mode == QGEMM_MODE_INT8 ? qg::FMT_INT8 : qg::FMT_INT4);
@@ -91,7 +119,7 @@ size_t rowsum_ws(int M, int K, int mode, int block, int a_dtype) {
 // sums are required; the tensor-core path's split-K partials are optional (with less scratch it
 // splits less), so `required` leaves them out.
 size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool required) {
-    if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K);
+    if (mode == QGEMM_MODE_W4A8) return w4a8_ws(M, K, N, block);
     const Path path = choose_path(M, K, N, mode, a_dtype);
     if (path == PATH_PREFILL) {
         const size_t rows = rowsum_ws(M, K, mode, block, a_dtype);
@@ -109,6 +137,8 @@ size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool requir
 }  // namespace
 
 int qg::option_overlap() { return g_opt_overlap.load(std::memory_order_relaxed); }
+long long qg::option_wait_ns() { return 1000LL * g_opt_wait_us.load(std::memory_order_relaxed); }
+int qg::option_stall() { return g_opt_stall.load(std::memory_order_relaxed); }
 
 int qg::api_fail(int code, const char* detail) { return fail(code, "%s", detail); }
 size_t qg::api_packed_bytes(int K, int N, int mode, int block, int w_dtype, size_t* table_bytes) {
@@ -134,6 +164,19 @@ int qgemm_set_option(int option, int value) {
         if (value != 0 && value != 1) return fail(QGEMM_ERR_ARG, "option %d takes 0 or 1, got %d", option, value);
         return g_opt_split_k.exchange(value);
     }
+    if (option == QGEMM_OPT_WAIT_LIMIT_US) {
+        if (value < 1 || value > 1000000)
+            return fail(QGEMM_ERR_ARG, "option %d takes 1..1000000 (microseconds), got %d", option, value);
+        return g_opt_wait_us.exchange(value);
+    }
+    if (option == QGEMM_OPT_DEBUG_STALL) {
+        if (value != 0 && value != 1) return fail(QGEMM_ERR_ARG, "option %d takes 0 or 1, got %d", option, value);
+        return g_opt_stall.exchange(value);
+    }
+    if (option == QGEMM_OPT_FAULT_INJECT) {
+        if (value < 0) return fail(QGEMM_ERR_ARG, "option %d takes a count >= 0, got %d", option, value);
+        return g_fault.exchange(value);
+    }
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
@@ -141,6 +184,9 @@ int qgemm_get_option(int option) {
     if (option == QGEMM_OPT_LAUNCH_OVERLAP) return g_opt_overlap.load();
     if (option == QGEMM_OPT_DECODE_MAX_M) return g_opt_decode_max_m.load();
     if (option == QGEMM_OPT_SPLIT_K) return g_opt_split_k.load();
+    if (option == QGEMM_OPT_WAIT_LIMIT_US) return g_opt_wait_us.load();
+    if (option == QGEMM_OPT_DEBUG_STALL) return g_opt_stall.load();
+    if (option == QGEMM_OPT_FAULT_INJECT) return g_fault.load();
     return fail(QGEMM_ERR_ARG, "unknown option %d", option);
 }
 
@@ -168,15 +214,18 @@ int qgemm_pack(const float* W, int K, int N, int mode, int block, int w_dtype, v
     if (N == 0) return QGEMM_OK;
     if (!W || !Bp) return fail(QGEMM_ERR_ARG, "null W or Bp");
     if (!aligned16(W) || !aligned16(Bp)) return fail(QGEMM_ERR_ALIGN, "W and Bp must be 16-byte aligned");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (mode == QGEMM_MODE_FLOAT) {
-        if (!valid_dtype(w_dtype)) return fail(QGEMM_ERR_ARG, "unknown w_dtype %d", w_dtype);
-        e = qg::launch_float_pack(W, K, N, w_dtype, Bp, s);
-    } else {
+    if (mode == QGEMM_MODE_FLOAT && !valid_dtype(w_dtype)) return fail(QGEMM_ERR_ARG, "unknown w_dtype %d", w_dtype);
+    if (mode != QGEMM_MODE_FLOAT) {
         if (!T) return fail(QGEMM_ERR_ARG, "null T");
         if (!aligned16(T)) return fail(QGEMM_ERR_ALIGN, "T must be 16-byte aligned");
         if ((size_t)(K / block) > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "too many blocks per channel");
+    }
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == QGEMM_MODE_FLOAT) {
+        e = qg::launch_float_pack(W, K, N, w_dtype, Bp, s);
+    } else {
         e = qg::launch_quant_pack(W, K, N, block, mode == QGEMM_MODE_INT8 ? 8 : 4, static_cast<uint8_t*>(Bp), T, s);
     }
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "qgemm_pack launch");
@@ -204,10 +253,13 @@ int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int
         (workspace && !aligned16(workspace)) || (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
         return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C, bias, residual and workspace must be 16-byte aligned");
     if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
+    if (mode == QGEMM_MODE_W4A8 && K > kW4A8MaxK)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A8 with K=%d could overflow the int32 accumulators", K);
     const size_t need = run_ws(M, K, N, mode, block, a_dtype, true);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     qg::Epilogue ep;
@@ -221,6 +273,19 @@ int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int
         int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
         e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
         if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+        if (w4a8_chunked(K, block)) {
+            // K-chunks whose float32 sums are exact integers, added in int32, then rescaled
+            int32_t* acc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(rs) + align256((size_t)M * 4));
+            e = cudaMemsetAsync(acc, 0, (size_t)M * N * sizeof(int32_t), s);
+            if (e != cudaSuccess) return cuda_fail(e, "accumulator clear");
+            qg::W4A8Args w{M, K, N, qa16, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
+            w.splits = qg::w4a8_exact_splits(K);
+            w.acc_add = 1;
+            e = qg::launch_w4a8_gemm(w, s);
+            if (e != cudaSuccess) return cuda_fail(e, "w4a8 gemm launch");
+            e = qg::launch_w4a8_rescale(M, N, acc, as, rs, T, ep, C, c_dtype, s);
+            return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 rescale launch");
+        }
         qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep, block};
         e = qg::launch_w4a8_gemm(w, s);
         return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
@@ -264,6 +329,7 @@ int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float*
     if (!A || !qa || !a_scale || !rowsum) return fail(QGEMM_ERR_ARG, "null pointer");
     if (!aligned16(A) || !aligned16(qa) || !aligned16(a_scale) || !aligned16(rowsum))
         return fail(QGEMM_ERR_ALIGN, "pointers must be 16-byte aligned");
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
     cudaError_t e =
         qg::launch_act_quant(M, K, A, a_dtype, qa, nullptr, a_scale, rowsum, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "act_quant launch");
@@ -280,6 +346,7 @@ int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_
     int rc = check_shape(K, N, QGEMM_MODE_W4A8, &block);
     if (rc != QGEMM_OK) return rc;
     if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
+    if (K > kW4A8MaxK) return fail(QGEMM_ERR_UNSUPPORTED, "K=%d could overflow the int32 accumulators", K);
     if (M == 0 || N == 0) return QGEMM_OK;
     if (!qa || !Bp || !acc) return fail(QGEMM_ERR_ARG, "null pointer");
     if (!aligned16(qa) || !aligned16(Bp) || !aligned16(acc) || (workspace && !aligned16(workspace)))
@@ -288,10 +355,17 @@ int qgemm_w4a8_acc(int M, int K, int N, const int8_t* qa, const void* Bp, int32_
     if (!workspace || workspace_bytes < need)
         return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = qg::launch_codes_to_f16(qa, workspace, (size_t)M * K, s);
     if (e != cudaSuccess) return cuda_fail(e, "codes_to_f16 launch");
     qg::W4A8Args w{M, K, N, workspace, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
+    w.splits = qg::w4a8_exact_splits(K);
+    if (w.splits > 1) {   // K-chunks, each exact in float32, added into acc in int32
+        e = cudaMemsetAsync(acc, 0, (size_t)M * N * sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "accumulator clear");
+        w.acc_add = 1;
+    }
     e = qg::launch_w4a8_gemm(w, s);
     return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
 }

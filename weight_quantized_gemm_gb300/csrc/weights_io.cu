@@ -16,6 +16,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <new>
 #include <vector>
 
 #include "../../include/qgemm.h"
@@ -208,32 +209,36 @@ int qgemm_load(const char* path, void* Bp, size_t Bp_bytes, float* T, size_t T_b
     if (rc != QGEMM_OK) return rc;
     if (Bp_bytes < h.bp_bytes || (h.t_bytes && (!T || T_bytes < h.t_bytes)))
         return qg::api_fail(QGEMM_ERR_ARG, "destination buffers are smaller than the file's Bp / T");
-    // the whole payload is checked before anything is written to the destination
+    // The payload is read once into host memory and its checksum verified there; only those
+    // verified bytes are then copied to the destination, so a file that changes while it is read
+    // cannot put unchecked data into Bp or T.
     const Crc32& crc = crc32();
-    std::vector<uint8_t> buf(kChunk);
-    uint32_t c = 0;
     const uint64_t total = h.bp_bytes + h.t_bytes;
+    std::vector<uint8_t> payload;
+    try {
+        payload.resize((size_t)total);
+    } catch (const std::bad_alloc&) {
+        return qg::api_fail(QGEMM_ERR_IO, "no host memory for the weight file's payload");
+    }
+    uint32_t c = 0;
     for (uint64_t o = 0; o < total; o += kChunk) {
         const size_t n = (size_t)(total - o < kChunk ? total - o : kChunk);
-        if (fread(buf.data(), 1, n, f.f) != n) return qg::api_fail(QGEMM_ERR_IO, "weight file is truncated");
-        c = crc.update(c, buf.data(), n);
+        if (fread(payload.data() + o, 1, n, f.f) != n) return qg::api_fail(QGEMM_ERR_IO, "weight file is truncated");
+        c = crc.update(c, payload.data() + o, n);
     }
     uint8_t extra;
     if (fread(&extra, 1, 1, f.f) != 0) return qg::api_fail(QGEMM_ERR_IO, "weight file has trailing bytes");
     if (c != h.crc) return qg::api_fail(QGEMM_ERR_IO, "weight file checksum mismatch");
-    if (fseek(f.f, kHeaderBytes, SEEK_SET) != 0) return qg::api_fail(QGEMM_ERR_IO, "seek failed");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const struct {
         void* p;
-        uint64_t n;
-    } parts[2] = {{Bp, h.bp_bytes}, {T, h.t_bytes}};
-    for (const auto& part : parts)
-        for (uint64_t o = 0; o < part.n; o += kChunk) {
-            const size_t n = (size_t)(part.n - o < kChunk ? part.n - o : kChunk);
-            if (fread(buf.data(), 1, n, f.f) != n) return qg::api_fail(QGEMM_ERR_IO, "weight file is truncated");
-            rc = copy_out(static_cast<uint8_t*>(part.p) + o, buf.data(), n, on_device, s);
-            if (rc != QGEMM_OK) return rc;
-        }
+        uint64_t off, n;
+    } parts[2] = {{Bp, 0, h.bp_bytes}, {T, h.bp_bytes, h.t_bytes}};
+    for (const auto& part : parts) {
+        if (part.n == 0) continue;
+        rc = copy_out(part.p, payload.data() + part.off, (size_t)part.n, on_device, s);
+        if (rc != QGEMM_OK) return rc;
+    }
     return QGEMM_OK;
 }
 
