@@ -75,11 +75,14 @@ KERNEL_SOURCES = {
     "decode": ["decode_stream.cuh", "decode_kernel.cuh", "decode_int4.cu", "decode_int8.cu", "decode_float.cu",
                "epilogue.cuh", "ptx.cuh", "internal.h"],
     "prefill": ["prefill_kernel.cuh", "prefill.cu", "prefill_codes.cu", "epilogue.cuh", "ptx.cuh", "internal.h"],
+    "f32": ["decode.cu", "epilogue.cuh", "internal.h"],
 }
 
 
 def kernel_of(w: synth.Workload) -> str:
-    return "decode" if (w.M <= 16 and w.mode != synth.MODE_W4A8 and w.a_dtype != synth.F32) else "prefill"
+    if w.a_dtype == synth.F32 and w.mode != synth.MODE_W4A8:
+        return "f32"      # the exact CUDA-core kernel
+    return "decode" if (w.M <= 16 and w.mode != synth.MODE_W4A8) else "prefill"
 
 
 def src_hash(kernel: str) -> str:
