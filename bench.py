@@ -355,7 +355,8 @@ def time_graph(g, stream, reps: int, dist, device) -> list[float]:
     synchronize on both sides and timed with CUDA events on the launching stream (max over
     ranks). One untimed replay first keeps the graph's own first-launch cost out."""
     import torch
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     stream.synchronize()
     out = []
     for _ in range(reps):
@@ -364,9 +365,10 @@ def time_graph(g, stream, reps: int, dist, device) -> list[float]:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        start.record(stream)
-        g.replay()
-        end.record(stream)
+        with torch.cuda.stream(stream):     # replay() launches on the current stream
+            start.record(stream)
+            g.replay()
+            end.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
         if dist is not None:
@@ -470,8 +472,9 @@ def run_headline(args, w: synth.Workload, device, stream, peaks: dict, dist, wor
         res["main"] = per_call(time_graph(graphs[main_mode], stream, args.reps, dist, device), args.steps)
         t_wall = time.perf_counter() - t_wall
         if t_wall < 1.0:    # keep the sampler running long enough to see the load (replays are identical)
-            for _ in range(min(int(1.0 / max(t_wall / args.reps, 1e-5)), 5000)):
-                graphs[main_mode].replay()
+            with torch.cuda.stream(stream):
+                for _ in range(min(int(1.0 / max(t_wall / args.reps, 1e-5)), 5000)):
+                    graphs[main_mode].replay()
             stream.synchronize()
     res["clocks"] = clk.summary()
     if w.mode == synth.MODE_W4A8:

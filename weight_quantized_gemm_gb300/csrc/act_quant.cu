@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace qg {
@@ -43,51 +45,69 @@ __device__ __forceinline__ void load8(const void* A, size_t i, float (&v)[8]) {
     }
 }
 
-// The codes of 8 values: RN-even of v * RN(1/s) unless one of them lies within 3e-5 of a
+// 1.5 * 2^23: for |y| < 2^22, y + kRound lies in [2^23, 2^24), where the float spacing is 1, so
+// the addition itself rounds y to an integer, ties to even, and that integer sits in the low
+// mantissa bits: (y + kRound) - kRound == rint(y) exactly, and for |rint(y)| <= 127 the low byte
+// of the sum's bit pattern is the code as an int8. This replaces a float-to-integer conversion
+// (a quarter-rate instruction) per element.
+constexpr float kRound = 12582912.0f;
+
+// The codes of 8 values: RN-even of y = RN(v * RN(1/s)) unless one of them lies within 3e-5 of a
 // half-integer (or the row's scale is subnormal: `exact`), then of the correctly rounded quotient
-// for all 8; clamped to +-127 (as rounded floats, exact); the f16 copies, the int8 bytes and the
-// running sum of the codes.
+// for all 8, clamped to +-127. With a normal scale no clamp is needed: s = RN(max|a| / 127) and
+// three roundings keep |y| below 127 (1 + 2^-24)^3 < 127.5, and |v / s| below 127 (1 + 2^-24).
+// Adds the chunk's code sum to `sum`; writes the f16 copies (H16) and the int8 bytes (Q8).
+template <bool H16, bool Q8>
 __device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rcp, bool exact, int& sum, uint4& h16,
                                           uint2& q8) {
-    float r[8];
+    float t[8];   // kRound + code
     float dev = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float y = v[j] * rcp;
-        r[j] = rintf(y);
-        dev = fmaxf(dev, fabsf(y - r[j]));   // distance to the nearest integer, <= 0.5
+        const float y = __fmul_rn(v[j], rcp);   // no contraction: y is the rounded product
+        t[j] = __fadd_rn(y, kRound);
+        dev = fmaxf(dev, fabsf(__fsub_rn(y, __fsub_rn(t[j], kRound))));   // distance to rint(y), <= 0.5
     }
     if (exact || dev > 0.49997f) {   // near a half-integer: decide by the exact quotient
 #pragma unroll
-        for (int j = 0; j < 8; ++j) r[j] = rintf(__fdiv_rn(v[j], s));
+        for (int j = 0; j < 8; ++j) t[j] = __fadd_rn(fminf(fmaxf(rintf(__fdiv_rn(v[j], s)), -127.f), 127.f), kRound);
     }
-    uint32_t hw[4];
+    float r[8];
     float cs = 0.f;   // the chunk's code sum, exact (|cs| <= 1016)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        r[j] = fminf(fmaxf(r[j], -127.f), 127.f);
+        r[j] = __fsub_rn(t[j], kRound);
         cs += r[j];
     }
     sum += __float2int_rn(cs);
+    if constexpr (H16) {
+        uint32_t hw[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 h = __floats2half2_rn(r[2 * j], r[2 * j + 1]);   // integers <= 127: exact
-        hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = __floats2half2_rn(r[2 * j], r[2 * j + 1]);   // integers <= 127: exact
+            hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        h16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
-    h16 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    uint32_t b[2] = {0u, 0u};
+    if constexpr (Q8) {
+        uint32_t b[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) b[j >> 2] |= ((uint32_t)__float2int_rn(r[j]) & 0xFFu) << (8 * (j & 3));
-    q8 = make_uint2(b[0], b[1]);
+        for (int w = 0; w < 2; ++w) {   // byte 0 of each of the four t's bit patterns
+            const uint32_t lo = __byte_perm(__float_as_uint(t[4 * w]), __float_as_uint(t[4 * w + 1]), 0x0040u);
+            const uint32_t hi = __byte_perm(__float_as_uint(t[4 * w + 2]), __float_as_uint(t[4 * w + 3]), 0x0040u);
+            b[w] = __byte_perm(lo, hi, 0x5410u);
+        }
+        q8 = make_uint2(b[0], b[1]);
+    }
 }
 
 // One block per row. The row is read once: each thread keeps up to kCache chunks of 8 values in
-// registers between the max pass and the quantize pass (K <= 8192); longer rows re-read the rest.
-template <int ADT>
+// registers between the max pass and the quantize pass (K <= 4096); longer rows re-read the rest.
+template <int ADT, bool H16, bool Q8>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* __restrict__ A,
                                                              int8_t* __restrict__ qa, __half* __restrict__ qa16,
                                                              float* __restrict__ as, int32_t* __restrict__ rowsum) {
-    constexpr int kCache = 4;
+    constexpr int kCache = 2;
     __shared__ float s_max[kThreads / 32];
     __shared__ int s_sum[kThreads / 32];
     const int m = blockIdx.x;
@@ -127,9 +147,9 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
     auto emit = [&](int k, const float (&w)[8]) {
         uint4 h16;
         uint2 q8;
-        quantize8(w, s, rcp, exact, sum, h16, q8);
-        if (qa16) *reinterpret_cast<uint4*>(qa16 + row + k) = h16;
-        if (qa) *reinterpret_cast<uint2*>(qa + row + k) = q8;
+        quantize8<H16, Q8>(w, s, rcp, exact, sum, h16, q8);
+        if constexpr (H16) *reinterpret_cast<uint4*>(qa16 + row + k) = h16;
+        if constexpr (Q8) *reinterpret_cast<uint2*>(qa + row + k) = q8;
     };
 #pragma unroll
     for (int i = 0; i < kCache; ++i) {
@@ -189,12 +209,21 @@ cudaError_t launch_row_sums(int M, int K, const void* A, int a_dtype, float* out
 cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
                              int32_t* rowsum, cudaStream_t s) {
     __half* h = static_cast<__half*>(qa16);
+    auto go = [&](auto adt) {
+        constexpr int ADT = decltype(adt)::value;
+        if (qa && h)
+            act_quant_kernel<ADT, true, true><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+        else if (h)
+            act_quant_kernel<ADT, true, false><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+        else
+            act_quant_kernel<ADT, false, true><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+    };
     if (a_dtype == DT_F32)
-        act_quant_kernel<DT_F32><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+        go(std::integral_constant<int, DT_F32>{});
     else if (a_dtype == DT_F16)
-        act_quant_kernel<DT_F16><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+        go(std::integral_constant<int, DT_F16>{});
     else
-        act_quant_kernel<DT_BF16><<<M, kThreads, 0, s>>>(K, A, qa, h, as, rowsum);
+        go(std::integral_constant<int, DT_BF16>{});
     return cudaGetLastError();
 }
 
