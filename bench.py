@@ -451,6 +451,67 @@ def bench_entry(w: synth.Workload, device, stream, peaks: dict, reps: int, dist,
     return out
 
 
+def bench_fused_pair(device, stream, reps: int, dist) -> dict:
+    """Two chained W4A8 layers of a 7B-class FFN, M=2048: the headline up-projection 4096 -> 14336,
+    then the down-projection 14336 -> 4096. Plain: the second layer quantizes its activations
+    itself (qgemm_run; rows of 14336 are longer than its register cache, so part of each row is
+    read twice); fused: the first layer's epilogue hands its row maxima to a one-read pass that
+    writes the codes (qgemm_run_fused_quant) and the second layer starts from them
+    (qgemm_run_w4a8_codes). Median per pair over `reps` replays."""
+    import torch
+
+    import weight_quantized_gemm_gb300 as qg
+    lib = qg.load()
+    w1 = synth.WORKLOADS["w4a8_m2048_k4096_n14336"]
+    w2 = synth.Workload("pair_down", 2048, 14336, 4096, synth.MODE_W4A8, 0, synth.BF16, synth.BF16, 0, 3)
+    l1, l2 = Layer(w1, device, stream), Layer(w2, device, stream)
+    M, K1, N1, N2 = w1.M, w1.K, w1.N, w2.N
+    C1 = torch.empty((M, N1), dtype=torch.bfloat16, device=device)
+    qa = torch.empty((M, N1), dtype=torch.float16, device=device)
+    asc = torch.empty(M, dtype=torch.float32, device=device)
+    rs = torch.empty(M, dtype=torch.int32, device=device)
+    fq = qg.qgemm_fused_quant_workspace_bytes(M, K1, N1, 3, 0, synth.BF16, synth.BF16)
+    ws1 = torch.empty(max(fq, l1.wsb, 16), dtype=torch.uint8, device=device)
+    wsc = qg.qgemm_w4a8_codes_workspace_bytes(M, N1, N2, 0)
+    ws2 = torch.empty(max(wsc, 16), dtype=torch.uint8, device=device)
+    s_ptr = stream.cuda_stream
+
+    def check(rc, what):
+        if rc != 0:
+            raise qg.QgemmError(rc, what)
+
+    def plain(i):
+        check(lib.qgemm_run(M, K1, N1, 3, 0, l1.As[i % len(l1.As)].data_ptr(), synth.BF16,
+                            l1.Bps[i % l1.copies].data_ptr(), l1.Ts[i % l1.copies].data_ptr(), C1.data_ptr(),
+                            synth.BF16, ws1.data_ptr(), l1.wsb, s_ptr), "layer 1")
+        check(lib.qgemm_run(M, N1, N2, 3, 0, C1.data_ptr(), synth.BF16, l2.Bps[i % l2.copies].data_ptr(),
+                            l2.Ts[i % l2.copies].data_ptr(), l2.C.data_ptr(), synth.BF16, l2.ws.data_ptr(), l2.wsb,
+                            s_ptr), "layer 2")
+
+    def fused(i):
+        check(lib.qgemm_run_fused_quant(M, K1, N1, 3, 0, l1.As[i % len(l1.As)].data_ptr(), synth.BF16,
+                                        l1.Bps[i % l1.copies].data_ptr(), l1.Ts[i % l1.copies].data_ptr(), None, 0,
+                                        None, C1.data_ptr(), synth.BF16, qa.data_ptr(), asc.data_ptr(), rs.data_ptr(),
+                                        ws1.data_ptr(), fq, s_ptr), "layer 1 (fused)")
+        check(lib.qgemm_run_w4a8_codes(M, N1, N2, 0, qa.data_ptr(), asc.data_ptr(), rs.data_ptr(),
+                                       l2.Bps[i % l2.copies].data_ptr(), l2.Ts[i % l2.copies].data_ptr(), None, 0,
+                                       None, l2.C.data_ptr(), synth.BF16, ws2.data_ptr(), wsc, s_ptr),
+              "layer 2 (codes)")
+
+    out = {"layers": "W4A8 M=2048: K=4096 -> N=14336, then K=14336 -> N=4096", "pairs_per_replay": 10}
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            plain(i)
+            fused(i)
+    stream.synchronize()
+    for name, fn in (("plain", plain), ("fused", fused)):
+        g = l1.graph(fn, 10, 0)
+        out[name + "_ms_per_pair"] = per_call(time_graph(g, stream, reps, dist, device), 10)["median_ms"]
+        del g
+    out["saved_ms_per_pair"] = out["plain_ms_per_pair"] - out["fused_ms_per_pair"]
+    return out
+
+
 def run_headline(args, w: synth.Workload, device, stream, peaks: dict, dist, world: int) -> dict:
     """The headline workload: K calls in one CUDA graph, replayed `reps` times (median and min
     per call), clocks sampled during the timed replays, the end-to-end rate through the public
@@ -697,6 +758,7 @@ def main():
             entries[key] = bench_entry(pw, device, stream, peaks, args.reps, dist, args.decode_max_m or 16,
                                        0.0 if args.no_cpu_baseline else 3.0, rank)
             torch.cuda.empty_cache()
+        entries["fused_act_quant_pair"] = bench_fused_pair(device, stream, args.reps, dist)
         line["per_config"] = entries
     if rank == 0:
         print(json.dumps(line))

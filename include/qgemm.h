@@ -154,6 +154,46 @@ int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int
                     const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---------------------------------------------------------------- activation step fused into the producer */
+
+/* A layer (as qgemm_run_fused) that also produces the next W4A8 layer's activation codes from its
+ * own output, so that a W4A8 layer fed by it skips its activation pass (the step on either side
+ * of the path: the W4A8 activation quantization of «测试用例与注册机制», applied where the previous
+ * layer's accumulators are still in float32, the Vulkan pull request's note on the DIRECT build).
+ * After C is written exactly as qgemm_run_fused writes it, the activation step of qgemm_act_quant
+ * is applied to C's stored values (rows of N elements):
+ *   as_next[m] = max_n |C[m][n]| / 127, qa_next[m][n] = clamp(rint(C[m][n] / as_next[m]), -127, 127),
+ *   rowsum_next[m] = sum_n qa_next[m][n]
+ * bit for bit what qgemm_act_quant gives for C. The codes are written as exact f16 integers
+ * [M][N] (the form qgemm_run_w4a8_codes reads), as_next float32 [M], rowsum_next int32 [M].
+ * Where the layer runs on the tensor-core kernel in one launch (M above QGEMM_OPT_DECODE_MAX_M
+ * with 16-bit activations, and W4A8 with K <= 8808), its epilogue records each 128-channel tile's
+ * row maxima of |C| in the workspace and one pass reads C once to write the codes; on the other
+ * paths the activation pass runs on C after the layer. N must be a multiple of 64 (it is the next
+ * layer's K). Workspace: qgemm_fused_quant_workspace_bytes (the tensor-core path does not split K
+ * in this call). Errors as qgemm_run_fused; QGEMM_ERR_UNSUPPORTED for N % 64 != 0. */
+int qgemm_run_fused_quant(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                          const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
+                          void* qa_next, float* as_next, int32_t* rowsum_next, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Workspace bytes of qgemm_run_fused_quant (0 for invalid arguments or when none is needed). */
+size_t qgemm_fused_quant_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype);
+
+/* A W4A8 layer from activation codes already computed (by qgemm_run_fused_quant): qa exact f16
+ * integers [M][K] in [-127, 127], a_scale float32 [M], rowsum int32 [M] (their sum per row).
+ * Computes what qgemm_run_fused computes in W4A8 mode after its activation pass:
+ * C = act(a_scale * (ws * acc + off * rowsum) + bias) + residual with acc = sum_k qa * q (per-channel
+ * weights, block = 0 or K; exact), or the per-block form for block-quantized weights. The workspace
+ * (qgemm_w4a8_codes_workspace_bytes) holds int32 accumulators [M][N] when the weights are per channel
+ * and K > 8808, and is otherwise not needed. */
+int qgemm_run_w4a8_codes(int M, int K, int N, int block, const void* qa, const float* a_scale, const int32_t* rowsum,
+                         const void* Bp, const float* T, const float* bias, int act, const void* residual, void* C,
+                         int c_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of qgemm_run_w4a8_codes (0 if none). */
+size_t qgemm_w4a8_codes_workspace_bytes(int M, int K, int N, int block);
+
 /* The W4A8 activation step alone (same page and section: "激活动态量化为 INT8"): per row of
  * A [M][K], as[m] = max|a| / 127 (float32), qa = clamp(rint(a / as), -127, 127) with ties
  * to even (all 0 when as == 0), rowsum[m] = sum_k qa. Outputs qa int8 [M][K], as float32 [M],

@@ -240,3 +240,30 @@ def test_wait_limit_and_stall_options():
     assert qg.qgemm_set_option(qg.OPT_DEBUG_STALL, 1) == 0
     assert qg.qgemm_set_option(qg.OPT_DEBUG_STALL, 0) == 1
     assert qg.load().qgemm_set_option(qg.OPT_DEBUG_STALL, 2) == -1
+
+
+def test_fused_quant_sizes_and_checks():
+    lib = qg.load()
+    # tensor-core route: the per-tile row maxima [ceil(N/128)][M] float32 after the layer's scratch
+    assert qg.qgemm_fused_quant_workspace_bytes(256, 1024, 512, qg.MODE_INT4, 64, qg.F16, qg.BF16) == 4 * 256 * 4
+    w4 = 2 * 64 * 1024 + 2 * 256
+    assert qg.qgemm_fused_quant_workspace_bytes(64, 1024, 512, qg.MODE_W4A8, 0, qg.BF16, qg.BF16) == w4 + 4 * 64 * 4
+    # decode path: the standalone activation pass on C needs nothing beyond the layer's own scratch
+    assert (qg.qgemm_fused_quant_workspace_bytes(8, 4096, 11008, qg.MODE_INT4, 64, qg.BF16, qg.BF16) ==
+            qg.qgemm_workspace_bytes(8, 4096, 11008, qg.MODE_INT4, 64, qg.BF16, qg.BF16))
+    assert qg.qgemm_fused_quant_workspace_bytes(256, 1024, 520, qg.MODE_INT4, 64, qg.F16, qg.BF16) == 0   # N % 64
+    run = lib.qgemm_run_fused_quant
+    args = lambda **kw: [kw.get(k, v) for k, v in dict(
+        M=256, K=1024, N=512, mode=1, block=64, A=FAKE, a_dtype=1, Bp=FAKE, T=FAKE, bias=None, act=0, res=None,
+        C=FAKE, c_dtype=2, qa=FAKE, asc=FAKE, rs=FAKE, ws=FAKE, wsb=1 << 20, stream=None).items()]
+    assert run(*args(N=520)) == -2                     # the next layer's K must be a multiple of 64
+    assert run(*args(qa=None)) == -1
+    assert run(*args(rs=FAKE + 4)) == -3
+    assert run(*args(wsb=16)) == -4
+    assert run(*args(M=0, A=None, C=None)) == 0
+    # the consumer's int32 accumulators when K needs exact chunks
+    assert qg.qgemm_w4a8_codes_workspace_bytes(16, 8832, 40, 0) == -(-16 * 40 * 4 // 256) * 256
+    assert qg.qgemm_w4a8_codes_workspace_bytes(16, 4096, 40, 0) == 0
+    codes = lib.qgemm_run_w4a8_codes
+    assert codes(4, 128, 8, 0, FAKE, None, FAKE, FAKE, FAKE, None, 0, None, FAKE, 2, None, 0, None) == -1
+    assert codes(4, 8832, 8, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None, FAKE, 2, None, 0, None) == -4

@@ -15,7 +15,8 @@ import os
 __all__ = [
     "QgemmError", "load", "qgemm_packed_bytes", "qgemm_table_bytes", "qgemm_workspace_bytes", "qgemm_pack",
     "qgemm_run", "qgemm_act_quant", "qgemm_w4a8_acc", "qgemm_w4a8_acc_workspace_bytes", "qgemm_status", "qgemm_error_string", "qgemm_last_error",
-    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "OPT_WAIT_LIMIT_US", "OPT_DEBUG_STALL", "OPT_FAULT_INJECT", "qgemm_run_fused", "qgemm_save", "qgemm_load_info", "qgemm_load", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "qgemm_set_option", "qgemm_get_option", "OPT_LAUNCH_OVERLAP", "OPT_DECODE_MAX_M", "OPT_SPLIT_K", "OPT_WAIT_LIMIT_US", "OPT_DEBUG_STALL", "OPT_FAULT_INJECT", "qgemm_run_fused", "qgemm_save", "qgemm_load_info", "qgemm_load", "ACT_NONE", "ACT_RELU", "ACT_SILU", "ACT_GELU_TANH", "qgemm_run_noalloc", "NOALLOC_SCRATCH_BYTES", "qgemm_run_fused_quant",
+    "qgemm_fused_quant_workspace_bytes", "qgemm_run_w4a8_codes", "qgemm_w4a8_codes_workspace_bytes",
     "MODE_FLOAT", "MODE_INT4", "MODE_INT8", "MODE_W4A8", "F32", "F16", "BF16", "LIB_PATH",
 ]
 
@@ -50,6 +51,10 @@ SIGNATURES = {
     "qgemm_w4a8_acc_workspace_bytes": ([_I, _I], _SZ),
     "qgemm_status": ([_P], _I),
     "qgemm_run_noalloc": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P], _I),
+    "qgemm_run_fused_quant": ([_I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P, _P, _SZ, _P], _I),
+    "qgemm_fused_quant_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], _SZ),
+    "qgemm_run_w4a8_codes": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _P, _SZ, _P], _I),
+    "qgemm_w4a8_codes_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "qgemm_save": ([ctypes.c_char_p, _I, _I, _I, _I, _I, _P, _P, _I, _P], _I),
     "qgemm_load_info": ([ctypes.c_char_p] + [ctypes.POINTER(ctypes.c_int)] * 5, _I),
     "qgemm_load": ([ctypes.c_char_p, _P, _SZ, _P, _SZ, _I, _P], _I),
@@ -179,6 +184,37 @@ def qgemm_run_noalloc(M: int, K: int, N: int, mode: int, block: int, A, a_dtype:
     """qgemm_run with the library's built-in scratch instead of a caller workspace (see qgemm.h)."""
     _check(load().qgemm_run_noalloc(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(C), c_dtype,
                                     _stream(stream)), "qgemm_run_noalloc")
+
+
+def qgemm_fused_quant_workspace_bytes(M: int, K: int, N: int, mode: int, block: int, a_dtype: int,
+                                      c_dtype: int) -> int:
+    return load().qgemm_fused_quant_workspace_bytes(M, K, N, mode, block, a_dtype, c_dtype)
+
+
+def qgemm_run_fused_quant(M: int, K: int, N: int, mode: int, block: int, A, a_dtype: int, Bp, T, bias, act: int,
+                          residual, C, c_dtype: int, qa_next, as_next, rowsum_next, workspace=None,
+                          workspace_bytes: int | None = None, stream=None) -> None:
+    """The layer (as qgemm_run_fused) plus the next W4A8 layer's activation codes of C (see qgemm.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().qgemm_run_fused_quant(M, K, N, mode, block, _ptr(A), a_dtype, _ptr(Bp), _ptr(T), _ptr(bias), act,
+                                        _ptr(residual), _ptr(C), c_dtype, _ptr(qa_next), _ptr(as_next),
+                                        _ptr(rowsum_next), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qgemm_run_fused_quant")
+
+
+def qgemm_w4a8_codes_workspace_bytes(M: int, K: int, N: int, block: int) -> int:
+    return load().qgemm_w4a8_codes_workspace_bytes(M, K, N, block)
+
+
+def qgemm_run_w4a8_codes(M: int, K: int, N: int, block: int, qa, a_scale, rowsum, Bp, T, bias, act: int, residual,
+                         C, c_dtype: int, workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    """A W4A8 layer from activation codes (exact f16), row scales and code sums (see qgemm.h)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().qgemm_run_w4a8_codes(M, K, N, block, _ptr(qa), _ptr(a_scale), _ptr(rowsum), _ptr(Bp), _ptr(T),
+                                       _ptr(bias), act, _ptr(residual), _ptr(C), c_dtype, _ptr(workspace),
+                                       workspace_bytes, _stream(stream)), "qgemm_run_w4a8_codes")
 
 
 def qgemm_act_quant(M: int, K: int, A, a_dtype: int, qa, a_scale, rowsum, stream=None) -> None:

@@ -174,6 +174,55 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
     }
 }
 
+// The next layer's activation step on a layer output C whose row maxima are already known per
+// 128-channel tile (the tensor-core epilogue wrote them): one block per row takes the max of its
+// tile maxima and quantizes the row in a single read, with the arithmetic of act_quant_kernel, so
+// the codes are the ones act_quant_kernel would give for C.
+template <int CDT>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(int N, const void* __restrict__ C,
+                                                              const float* __restrict__ rowmax, int ntiles, int M,
+                                                              __half* __restrict__ qa16, float* __restrict__ as,
+                                                              int32_t* __restrict__ rowsum) {
+    __shared__ int s_sum[kThreads / 32];
+    const int m = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t row = (size_t)m * N;
+    float amax = 0.f;
+    for (int t = lane; t < ntiles; t += 32) amax = fmaxf(amax, __ldg(rowmax + (size_t)t * M + m));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = __fdiv_rn(amax, 127.0f);
+    const bool exact = s != 0.f && s < 1.17549435e-38f;
+    const float rcp = (s != 0.f && !exact) ? __frcp_rn(s) : 0.f;
+    int sum = 0;
+    // two chunks per thread and step, both requested before either is quantized
+    for (int k0 = threadIdx.x * 8; k0 < N; k0 += 2 * kThreads * 8) {
+        const int k1 = k0 + kThreads * 8;
+        float v0[8], v1[8];
+        load8<CDT>(C, row + k0, v0);
+        if (k1 < N) load8<CDT>(C, row + k1, v1);
+        uint4 h16;
+        uint2 q8;
+        quantize8<true, false>(v0, s, rcp, exact, sum, h16, q8);
+        *reinterpret_cast<uint4*>(qa16 + row + k0) = h16;
+        if (k1 < N) {
+            quantize8<true, false>(v1, s, rcp, exact, sum, h16, q8);
+            *reinterpret_cast<uint4*>(qa16 + row + k1) = h16;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) s_sum[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) total += s_sum[w];
+        as[m] = s;
+        rowsum[m] = total;
+    }
+}
+
 // Row sums of A in float32 (the Int8-Block0 tensor-core path's offset term o * sum_k a): one
 // warp per row, 8 consecutive values per lane and step (16-byte loads), a shuffle reduction.
 template <int ADT>
@@ -203,6 +252,18 @@ cudaError_t launch_row_sums(int M, int K, const void* A, int a_dtype, float* out
         row_sum_kernel<DT_F16><<<blocks, kThreads, 0, s>>>(M, K, A, out);
     else
         row_sum_kernel<DT_BF16><<<blocks, kThreads, 0, s>>>(M, K, A, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(int M, int N, const void* C, int c_dtype, const float* rowmax, int ntiles,
+                              void* qa16, float* as, int32_t* rowsum, cudaStream_t s) {
+    __half* h = static_cast<__half*>(qa16);
+    if (c_dtype == DT_F32)
+        quant_rows_kernel<DT_F32><<<M, kThreads, 0, s>>>(N, C, rowmax, ntiles, M, h, as, rowsum);
+    else if (c_dtype == DT_F16)
+        quant_rows_kernel<DT_F16><<<M, kThreads, 0, s>>>(N, C, rowmax, ntiles, M, h, as, rowsum);
+    else
+        quant_rows_kernel<DT_BF16><<<M, kThreads, 0, s>>>(N, C, rowmax, ntiles, M, h, as, rowsum);
     return cudaGetLastError();
 }
 

@@ -80,6 +80,7 @@ struct PrefillArgs {
     int splits;       // K-splits across thread blocks (>= 1), from prefill_splits
     Epilogue ep;
     float* rowsum;    // [M] scratch for the row sums of A (Int8-Block0 on the codes path)
+    float* rowmax = nullptr;   // [ceil(N/128)][M] per-tile row maxima of |C| (no K-split), or none
 };
 // Int8-Block0 (per-channel) layers with bf16 activations and M >= 256 run on the tensor cores as
 // raw codes with the scale and offset applied in the epilogue (they need [M] float32 row sums of A
@@ -99,6 +100,11 @@ bool prefill_supported(int M, int K, int N, int fmt, int a_dtype);
 cudaError_t launch_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, void* qa16, float* as,
                              int32_t* rowsum, cudaStream_t s);
 cudaError_t launch_codes_to_f16(const int8_t* qa, void* out, size_t n, cudaStream_t s);
+// The activation step of a next W4A8 layer applied to C [M][N] (c_dtype) when the row maxima of
+// |C| are known per 128-channel tile (rowmax [ntiles][M], from the tensor-core epilogue): codes as
+// exact f16 [M][N], scales and code sums; the same codes as launch_act_quant on C. N % 8 == 0.
+cudaError_t launch_quant_rows(int M, int N, const void* C, int c_dtype, const float* rowmax, int ntiles,
+                              void* qa16, float* as, int32_t* rowsum, cudaStream_t s);
 // out[m] = sum_k A[m][k] in float32 (the Int8-Block0 tensor-core path's row sums)
 cudaError_t launch_row_sums(int M, int K, const void* A, int a_dtype, float* out, cudaStream_t s);
 // acc (int32 [M][N]) = qa x q^T; or, when acc == nullptr, the rescaled output into C.
@@ -116,6 +122,7 @@ struct W4A8Args {
     int block = 0;  // K-block of the weights' {offset, scale} (0 or K: per channel)
     int splits = 1; // K-chunks (grid z); with acc_add each chunk adds its int32 sums into acc
     int acc_add = 0;
+    float* rowmax = nullptr;   // [ceil(N/128)][M] per-tile row maxima of |C| (rescaled output only)
 };
 cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s);
 // The integer sums of the W4A8 tensor-core GEMM are exact while every float32 partial sum is an

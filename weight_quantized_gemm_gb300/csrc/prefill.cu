@@ -88,6 +88,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     p.wait_ns = option_wait_ns();
     p.stall = option_stall();
     p.ep = p.splits > 1 ? Epilogue{} : a.ep;   // split partials: the reduction applies it
+    p.rowmax = p.splits > 1 ? nullptr : a.rowmax;
     // with K-splits the kernel writes float32 partial sums [splits][M][N], reduced in fixed order
     const int kdt = p.splits > 1 ? DT_F32 : a.c_dtype;
     if (p.splits > 1) p.C = a.partial;

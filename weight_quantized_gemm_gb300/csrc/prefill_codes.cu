@@ -62,6 +62,7 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     p.wait_ns = option_wait_ns();
     p.stall = option_stall();
     p.ep = a.acc ? Epilogue{} : a.ep;
+    p.rowmax = a.acc ? nullptr : a.rowmax;
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
     if (e != cudaSuccess) return e;

@@ -80,6 +80,9 @@ struct Params {
     Epilogue ep;              // bias / activation / residual (none when the output is split partials)
     long long wait_ns;        // bound of each pipeline wait (waits that drain issued work: ptx::kWaitNs)
     int stall;                // diagnostic: the MMA issuer first waits on a barrier nothing arrives at
+    float* rowmax;            // when set (no K-split): rowmax[x * M + m] = max over the tile's channels of
+                              // |C[m][n]| as rounded to C's type, x = blockIdx.x (the next layer's
+                              // activation quantization takes the row max from these)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -707,6 +710,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
             }
         }
+        }
+        // Params::rowmax: the max over the tile's channels of each staged row (the values as stored
+        // in C's type), read back from the staged tile after the epilogue warps' barrier that both
+        // branches above passed. Each lane owns one row and visits its 128 channels in 32 groups of
+        // 4, starting at group `lane` (the lanes of a warp then read different banks); the loads
+        // are independent, so the pass is a few hundred cycles. It only reads shared memory and may
+        // overlap the tile's TMA store.
+        if constexpr (EPI != EPI_ACC) {
+            const int ml = (warp - 2) * 32 + lane;
+            if (p.rowmax && ok && warp - 2 < BN / 32 && ml < min(BN, p.M - m_tile)) {
+                const int nvalid = min(kBM, p.N - n_tile);
+                float mx = 0.f;
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int c = 4 * ((j + lane) & 31);
+                    float v[4];
+                    if constexpr (kEsz == 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(tile + ((size_t)ml * kBM + c) * 4);
+                        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+                    } else {
+                        const uint2 x = *reinterpret_cast<const uint2*>(tile + ((size_t)ml * kBM + c) * 2);
+                        const uint32_t w[2] = {x.x, x.y};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const unsigned short b = (unsigned short)(w[e >> 1] >> (16 * (e & 1)));
+                            v[e] = CDT == DT_F16 ? __half2float(__ushort_as_half(b)) : __uint_as_float((uint32_t)b << 16);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (c + e < nvalid) mx = fmaxf(mx, fabsf(v[e]));
+                }
+                p.rowmax[(size_t)blockIdx.x * p.M + m_tile + ml] = mx;
+            }
         }
     }
     tc_fence_before();

@@ -134,6 +134,125 @@ size_t run_ws(int M, int K, int N, int mode, int block, int a_dtype, bool requir
     return splits > 1 ? (size_t)splits * mc * N * sizeof(float) : 0;
 }
 
+// Checks shared by the layer calls (block normalised); QGEMM_OK for an empty call too.
+int check_run(int M, int K, int N, int mode, int* block, const void* A, int a_dtype, const void* Bp, const float* T,
+              const float* bias, int act, const void* residual, const void* C, int c_dtype, const void* workspace) {
+    int rc = check_shape(K, N, mode, block);
+    if (rc != QGEMM_OK) return rc;
+    if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
+    if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
+        return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
+    if (act < QGEMM_ACT_NONE || act > QGEMM_ACT_GELU_TANH) return fail(QGEMM_ERR_ARG, "unknown activation %d", act);
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (!A || !Bp || !C) return fail(QGEMM_ERR_ARG, "null A, Bp or C");
+    if (mode != QGEMM_MODE_FLOAT && !T) return fail(QGEMM_ERR_ARG, "null T");
+    if (!aligned16(A) || !aligned16(Bp) || !aligned16(C) || (T && !aligned16(T)) ||
+        (workspace && !aligned16(workspace)) || (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
+        return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C, bias, residual and workspace must be 16-byte aligned");
+    if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
+    if (mode == QGEMM_MODE_W4A8 && K > kW4A8MaxK)
+        return fail(QGEMM_ERR_UNSUPPORTED, "W4A8 with K=%d could overflow the int32 accumulators", K);
+    return QGEMM_OK;
+}
+
+qg::Epilogue make_ep(const float* bias, int act, const void* residual) {
+    qg::Epilogue ep;
+    ep.bias = bias;
+    ep.residual = residual;
+    ep.act = act;
+    return ep;
+}
+
+// The W4A8 GEMM from activation codes (exact f16 [M][K]), row scales and code sums: one launch,
+// or (per-channel weights, K past the exact range) int32 K-chunks added in acc_ws [M][N], then the
+// rescale. rowmax (one launch only): the epilogue's per-tile row maxima of |C|.
+int w4a8_from_codes(int M, int K, int N, int block, const void* qa16, const float* as, const int32_t* rs,
+                    const void* Bp, const float* T, const qg::Epilogue& ep, void* C, int c_dtype, int32_t* acc_ws,
+                    float* rowmax, cudaStream_t s) {
+    cudaError_t e;
+    if (w4a8_chunked(K, block)) {
+        e = cudaMemsetAsync(acc_ws, 0, (size_t)M * N * sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e, "accumulator clear");
+        qg::W4A8Args w{M, K, N, qa16, nullptr, nullptr, Bp, nullptr, acc_ws, nullptr, QGEMM_F32};
+        w.splits = qg::w4a8_exact_splits(K);
+        w.acc_add = 1;
+        e = qg::launch_w4a8_gemm(w, s);
+        if (e != cudaSuccess) return cuda_fail(e, "w4a8 gemm launch");
+        e = qg::launch_w4a8_rescale(M, N, acc_ws, as, rs, T, ep, C, c_dtype, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 rescale launch");
+    }
+    qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep, block};
+    w.rowmax = rowmax;
+    e = qg::launch_w4a8_gemm(w, s);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
+}
+
+// The launches of one layer call (every check done). rowmax: when set, the tensor-core epilogue
+// writes its per-tile row maxima of |C| there, and the call does not split K.
+int launch_layer(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                 const float* T, const qg::Epilogue& ep, void* C, int c_dtype, void* workspace, size_t workspace_bytes,
+                 float* rowmax, cudaStream_t s) {
+    cudaError_t e;
+    if (mode == QGEMM_MODE_W4A8) {
+        void* qa16 = workspace;
+        float* as = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)M * K * 2));
+        int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
+        e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
+        if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+        int32_t* acc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(rs) + align256((size_t)M * 4));
+        return w4a8_from_codes(M, K, N, block, qa16, as, rs, Bp, T, ep, C, c_dtype, acc, rowmax, s);
+    }
+    const int fmt = fmt_of(mode);
+    const Path path = choose_path(M, K, N, mode, a_dtype);
+    if (path == PATH_PREFILL) {
+        const size_t rows = rowsum_ws(M, K, mode, block, a_dtype);   // [row sums][split-K partials]
+        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C,
+                           rows ? reinterpret_cast<float*>(static_cast<char*>(workspace) + rows)
+                                : static_cast<float*>(workspace),
+                           1, ep, static_cast<float*>(workspace)};
+        pa.splits = rowmax ? 1 : prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes - rows : 0);
+        pa.rowmax = rowmax;
+        e = qg::launch_prefill(pa, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
+    }
+    qg::DecodeArgs da{};
+    da.M = M; da.K = K; da.N = N; da.block = block; da.fmt = fmt;
+    da.a_dtype = a_dtype; da.c_dtype = c_dtype;
+    da.A = A; da.Bp = Bp; da.T = T; da.C = C;
+    da.ep = ep;
+    if (path == PATH_F32) {
+        da.splits = 1;
+        e = qg::launch_decode_f32(da, s);
+        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode_f32 launch");
+    }
+    da.splits = 1;   // chosen per 16-row launch inside launch_decode
+    da.overlap = qg::option_overlap();
+    da.partial = static_cast<float*>(workspace);
+    e = qg::launch_decode(da, s);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode launch");
+}
+
+// Workspace of qgemm_run_fused_quant: the layer's own required scratch (no tensor-core K-split),
+// then, where the layer runs on the tensor-core kernel in one launch, the per-tile row maxima
+// [ceil(N/128)][M] float32 (256-byte aligned).
+struct FqLayout {
+    bool rowmax;
+    size_t parts_off, total;
+};
+FqLayout fq_layout(int M, int K, int N, int mode, int block, int a_dtype) {
+    FqLayout L{};
+    L.rowmax = mode == QGEMM_MODE_W4A8 ? !w4a8_chunked(K, block)
+                                       : choose_path(M, K, N, mode, a_dtype) == PATH_PREFILL;
+    const size_t layer = run_ws(M, K, N, mode, block, a_dtype, true);
+    if (!L.rowmax) {
+        L.total = layer;
+        return L;
+    }
+    L.parts_off = align256(layer);
+    L.total = L.parts_off + align256((size_t)((N + 127) / 128) * M * sizeof(float));
+    return L;
+}
+
 }  // namespace
 
 int qg::option_overlap() { return g_opt_overlap.load(std::memory_order_relaxed); }
@@ -240,84 +359,74 @@ int qgemm_run(int M, int K, int N, int mode, int block, const void* A, int a_dty
 int qgemm_run_fused(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
                     const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    int rc = check_shape(K, N, mode, &block);
-    if (rc != QGEMM_OK) return rc;
-    if (M < 0) return fail(QGEMM_ERR_ARG, "negative M=%d", M);
-    if (!valid_dtype(a_dtype) || !valid_dtype(c_dtype))
-        return fail(QGEMM_ERR_ARG, "unknown dtype (a_dtype %d, c_dtype %d)", a_dtype, c_dtype);
-    if (act < QGEMM_ACT_NONE || act > QGEMM_ACT_GELU_TANH) return fail(QGEMM_ERR_ARG, "unknown activation %d", act);
-    if (M == 0 || N == 0) return QGEMM_OK;
-    if (!A || !Bp || !C) return fail(QGEMM_ERR_ARG, "null A, Bp or C");
-    if (mode != QGEMM_MODE_FLOAT && !T) return fail(QGEMM_ERR_ARG, "null T");
-    if (!aligned16(A) || !aligned16(Bp) || !aligned16(C) || (T && !aligned16(T)) ||
-        (workspace && !aligned16(workspace)) || (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
-        return fail(QGEMM_ERR_ALIGN, "A, Bp, T, C, bias, residual and workspace must be 16-byte aligned");
-    if ((M + 15) / 16 > 65535) return fail(QGEMM_ERR_UNSUPPORTED, "M=%d exceeds the launch limit", M);
-    if (mode == QGEMM_MODE_W4A8 && K > kW4A8MaxK)
-        return fail(QGEMM_ERR_UNSUPPORTED, "W4A8 with K=%d could overflow the int32 accumulators", K);
+    int rc = check_run(M, K, N, mode, &block, A, a_dtype, Bp, T, bias, act, residual, C, c_dtype, workspace);
+    if (rc != QGEMM_OK || M == 0 || N == 0) return rc;
     const size_t need = run_ws(M, K, N, mode, block, a_dtype, true);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
     if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
+    return launch_layer(M, K, N, mode, block, A, a_dtype, Bp, T, make_ep(bias, act, residual), C, c_dtype, workspace,
+                        workspace_bytes, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t qgemm_fused_quant_workspace_bytes(int M, int K, int N, int mode, int block, int a_dtype, int c_dtype) {
+    if (M <= 0 || check_shape(K, N, mode, &block) != QGEMM_OK || !valid_dtype(a_dtype) || !valid_dtype(c_dtype) ||
+        N % 64 != 0)
+        return 0;
+    return fq_layout(M, K, N, mode, block, a_dtype).total;
+}
+
+int qgemm_run_fused_quant(int M, int K, int N, int mode, int block, const void* A, int a_dtype, const void* Bp,
+                          const float* T, const float* bias, int act, const void* residual, void* C, int c_dtype,
+                          void* qa_next, float* as_next, int32_t* rowsum_next, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    int rc = check_run(M, K, N, mode, &block, A, a_dtype, Bp, T, bias, act, residual, C, c_dtype, workspace);
+    if (rc != QGEMM_OK) return rc;
+    if (N % 64 != 0)
+        return fail(QGEMM_ERR_UNSUPPORTED, "N=%d: the next layer's K must be a multiple of 64", N);
+    if (M == 0 || N == 0) return QGEMM_OK;
+    if (!qa_next || !as_next || !rowsum_next) return fail(QGEMM_ERR_ARG, "null qa_next, as_next or rowsum_next");
+    if (!aligned16(qa_next) || !aligned16(as_next) || !aligned16(rowsum_next))
+        return fail(QGEMM_ERR_ALIGN, "qa_next, as_next and rowsum_next must be 16-byte aligned");
+    const FqLayout L = fq_layout(M, K, N, mode, block, a_dtype);
+    if (L.total > 0 && (!workspace || workspace_bytes < L.total))
+        return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    qg::Epilogue ep;
-    ep.bias = bias;
-    ep.residual = residual;
-    ep.act = act;
+    float* parts = L.rowmax ? reinterpret_cast<float*>(static_cast<char*>(workspace) + L.parts_off) : nullptr;
+    rc = launch_layer(M, K, N, mode, block, A, a_dtype, Bp, T, make_ep(bias, act, residual), C, c_dtype, workspace,
+                      L.rowmax ? L.parts_off : workspace_bytes, parts, s);
+    if (rc != QGEMM_OK) return rc;
+    // the next layer's activation step on C: from the epilogue's row maxima (one read of C), or,
+    // where the layer's kernel has no such epilogue, the standalone pass (same codes)
+    const cudaError_t e =
+        L.rowmax ? qg::launch_quant_rows(M, N, C, c_dtype, parts, (N + 127) / 128, qa_next, as_next, rowsum_next, s)
+                 : qg::launch_act_quant(M, N, C, c_dtype, nullptr, qa_next, as_next, rowsum_next, s);
+    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "activation step launch");
+}
 
-    if (mode == QGEMM_MODE_W4A8) {
-        void* qa16 = workspace;
-        float* as = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256((size_t)M * K * 2));
-        int32_t* rs = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(as) + align256((size_t)M * 4));
-        e = qg::launch_act_quant(M, K, A, a_dtype, nullptr, qa16, as, rs, s);
-        if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-        if (w4a8_chunked(K, block)) {
-            // K-chunks whose float32 sums are exact integers, added in int32, then rescaled
-            int32_t* acc = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(rs) + align256((size_t)M * 4));
-            e = cudaMemsetAsync(acc, 0, (size_t)M * N * sizeof(int32_t), s);
-            if (e != cudaSuccess) return cuda_fail(e, "accumulator clear");
-            qg::W4A8Args w{M, K, N, qa16, nullptr, nullptr, Bp, nullptr, acc, nullptr, QGEMM_F32};
-            w.splits = qg::w4a8_exact_splits(K);
-            w.acc_add = 1;
-            e = qg::launch_w4a8_gemm(w, s);
-            if (e != cudaSuccess) return cuda_fail(e, "w4a8 gemm launch");
-            e = qg::launch_w4a8_rescale(M, N, acc, as, rs, T, ep, C, c_dtype, s);
-            return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 rescale launch");
-        }
-        qg::W4A8Args w{M, K, N, qa16, as, rs, Bp, T, nullptr, C, c_dtype, ep, block};
-        e = qg::launch_w4a8_gemm(w, s);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "w4a8 gemm launch");
-    }
+size_t qgemm_w4a8_codes_workspace_bytes(int M, int K, int N, int block) {
+    if (M <= 0 || check_shape(K, N, QGEMM_MODE_W4A8, &block) != QGEMM_OK) return 0;
+    return w4a8_chunked(K, block) ? align256((size_t)M * N * 4) : 0;
+}
 
-    const int fmt = fmt_of(mode);
-    const Path path = choose_path(M, K, N, mode, a_dtype);
-    if (path == PATH_PREFILL) {
-        const size_t rows = rowsum_ws(M, K, mode, block, a_dtype);   // [row sums][split-K partials]
-        qg::PrefillArgs pa{M, K, N, block, fmt, a_dtype, c_dtype, A, Bp, T, C,
-                           rows ? reinterpret_cast<float*>(static_cast<char*>(workspace) + rows)
-                                : static_cast<float*>(workspace),
-                           1, ep, static_cast<float*>(workspace)};
-        pa.splits = prefill_splits_for(M, K, N, mode, workspace ? workspace_bytes - rows : 0);
-        e = qg::launch_prefill(pa, s);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "prefill launch");
-    }
-    qg::DecodeArgs da{};
-    da.M = M; da.K = K; da.N = N; da.block = block; da.fmt = fmt;
-    da.a_dtype = a_dtype; da.c_dtype = c_dtype;
-    da.A = A; da.Bp = Bp; da.T = T; da.C = C;
-    da.ep = ep;
-    if (path == PATH_F32) {
-        da.splits = 1;
-        e = qg::launch_decode_f32(da, s);
-        return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode_f32 launch");
-    }
-    da.splits = 1;   // chosen per 16-row launch inside launch_decode
-    da.overlap = qg::option_overlap();
-    da.partial = static_cast<float*>(workspace);
-    e = qg::launch_decode(da, s);
-    return e == cudaSuccess ? QGEMM_OK : cuda_fail(e, "decode launch");
+int qgemm_run_w4a8_codes(int M, int K, int N, int block, const void* qa, const float* a_scale, const int32_t* rowsum,
+                         const void* Bp, const float* T, const float* bias, int act, const void* residual, void* C,
+                         int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    int rc = check_run(M, K, N, QGEMM_MODE_W4A8, &block, qa, QGEMM_F16, Bp, T, bias, act, residual, C, c_dtype,
+                       workspace);
+    if (rc != QGEMM_OK || M == 0 || N == 0) return rc;
+    if (!a_scale || !rowsum) return fail(QGEMM_ERR_ARG, "null a_scale or rowsum");
+    if (!aligned16(a_scale) || !aligned16(rowsum)) return fail(QGEMM_ERR_ALIGN, "a_scale and rowsum must be 16-byte aligned");
+    const size_t need = w4a8_chunked(K, block) ? align256((size_t)M * N * 4) : 0;
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(QGEMM_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (inject_fault()) return fail(QGEMM_ERR_CUDA, "simulated launch failure (fault injection)");
+    return w4a8_from_codes(M, K, N, block, qa, a_scale, rowsum, Bp, T, make_ep(bias, act, residual), C, c_dtype,
+                           static_cast<int32_t*>(workspace), nullptr, static_cast<cudaStream_t>(stream));
 }
 
 int qgemm_act_quant(int M, int K, const void* A, int a_dtype, int8_t* qa, float* a_scale, int32_t* rowsum,
