@@ -76,12 +76,15 @@ struct Params {
     int r_tma;                // the epilogue's residual tile comes in by one TMA load (Maps::r)
     int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
     int tblocks;              // K-blocks per table box (min(SUB, nb))
+    int m_tiles;              // row tiles (ceil(M / BN)); the grid's x enumerates (channel tile, row tile)
+    int group_n;              // channel tiles per raster group (row tiles run fastest inside a group);
+                              // 0: channel tiles fastest over the whole grid
     unsigned int* status;     // the library's device status word (bounded waits that gave up)
     Epilogue ep;              // bias / activation / residual (none when the output is split partials)
     long long wait_ns;        // bound of each pipeline wait (waits that drain issued work: ptx::kWaitNs)
     int stall;                // diagnostic: the MMA issuer first waits on a barrier nothing arrives at
     float* rowmax;            // when set (no K-split): rowmax[x * M + m] = max over the tile's channels of
-                              // |C[m][n]| as rounded to C's type, x = blockIdx.x (the next layer's
+                              // |C[m][n]| as rounded to C's type, x = the tile's channel tile (the next layer's
                               // activation quantization takes the row max from these)
 };
 
@@ -314,6 +317,7 @@ constexpr size_t kSmemMax = 232448;                 // opt-in shared memory per 
 constexpr int kTail = 256 + kMaxBN * 8;              // barriers + W4A8 row factors after the ring
 constexpr int kRing = (int)kSmemMax - kTail;         // bytes for the stages
 constexpr int kMaxStages = 8;
+constexpr size_t kL2GroupBytes = 64u << 20;         // weights above this take the grouped raster
 template <int WF>
 struct WBox {   // bytes of one channel row of one 64-wide sub-stage
     static constexpr int kRowBytes =
@@ -378,7 +382,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t kABytes = (uint32_t)BN * kBK * 2;   // one activation box
     constexpr uint32_t w_off = SUB * kABytes, t_off = w_off + G::kWBytes;
-    const int n_tile = blockIdx.x * kBM, m_tile = blockIdx.y * BN;
+    // Raster. Weights larger than the L2 share: groups of group_n channel tiles with the row tiles
+    // fastest inside a group, so the blocks running at the same time share each weight tile (read
+    // from HBM once) and re-read only the activations, which stay in L2. Otherwise channel tiles
+    // fastest (group_n == 0): the weights stay in L2 and each activation tile is read by a run of
+    // consecutive blocks.
+    int n_idx, m_idx;
+    if (p.group_n > 0) {
+        const int per_group = p.group_n * p.m_tiles;
+        const int grp = (int)blockIdx.x / per_group, in_grp = (int)blockIdx.x - grp * per_group;
+        // (the last group may hold fewer channel tiles; the grid covers exactly n_tiles x m_tiles)
+        n_idx = grp * p.group_n + in_grp / p.m_tiles;
+        m_idx = in_grp % p.m_tiles;
+    } else {
+        const int n_tiles = (p.N + kBM - 1) / kBM;
+        n_idx = (int)blockIdx.x % n_tiles;
+        m_idx = (int)blockIdx.x / n_tiles;
+    }
+    const int n_tile = n_idx * kBM, m_tile = m_idx * BN;
     const int nsub = p.K / kBK;                        // 64-wide sub-stages of K
     const int nst = (nsub + SUB - 1) / SUB;            // stages (the last may be half past K: reads 0)
     // split z covers stages [ks0, ks0 + nks); the ring counts stages from 0 within the split
@@ -742,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     for (int e = 0; e < 4; ++e)
                         if (c + e < nvalid) mx = fmaxf(mx, fabsf(v[e]));
                 }
-                p.rowmax[(size_t)blockIdx.x * p.M + m_tile + ml] = mx;
+                p.rowmax[(size_t)n_idx * p.M + m_tile + ml] = mx;
             }
         }
     }
@@ -854,7 +875,7 @@ cudaError_t launch_k(const Maps& maps, const Params& p, cudaStream_t s) {
     auto kern = prefill_kernel<WF, BF, EPI, CDT, BN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kBM - 1) / kBM, (p.M + p.BN - 1) / p.BN, p.splits);
+    dim3 grid(((p.N + kBM - 1) / kBM) * p.m_tiles, 1, p.splits);
     kern<<<grid, kThreads, kSmemMax, s>>>(maps, p);
     return cudaGetLastError();
 }
@@ -867,6 +888,12 @@ cudaError_t launch_bn(Maps maps, Params p, int c_dtype, cudaStream_t s) {
     cudaError_t e = make_wmap(&maps.w, p.Bp, WF, BF, p.N, p.K, P::kSub);
     if (e != cudaSuccess) return e;
     p.tblocks = P::kSub < p.nb ? P::kSub : p.nb;
+    p.m_tiles = (p.M + BN - 1) / BN;
+    // weights beyond half the L2 (measured: the 117 MB f16 weights of a 4096 x 14336 layer were read
+    // about six times over with channel tiles fastest): row tiles fastest in groups of about two
+    // waves of blocks
+    const size_t wbytes = (size_t)p.N * p.K * WBox<WF>::kRowBytes / kBK;   // packed weight bytes
+    p.group_n = wbytes > kL2GroupBytes ? ((2 * kTargetSms) / p.m_tiles > 1 ? (2 * kTargetSms) / p.m_tiles : 1) : 0;
     if constexpr (P::G::kTable) e = make_table_map(&maps.t, p.T, p.N, p.nb, p.tblocks);
     else maps.t = maps.w;   // unused
     if (e != cudaSuccess) return e;
