@@ -374,6 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr bool kDequant = WF != WF_FLOAT;          // weights go through the dequant warps into TMEM
     constexpr int kRowB = WBox<WF>::kRowBytes;
     constexpr int kLo = SUB * 32;                      // TMEM column of the low parts in an A stage (Split)
+    // The packed weight box ([128 channel rows][SUB * kRowB bytes]) lands with the TMA swizzle whose
+    // span is one row (32, 64 or 128 bytes): the 16-byte chunk index is XOR-ed with address bits
+    // 7 and up, so the dequant warps' 16-byte reads of consecutive rows spread over all banks
+    // instead of 4 rows sharing each 128-byte line's banks.
+    constexpr uint32_t kWSwMask = (uint32_t)(SUB * kRowB) / 16u - 1u;
+    auto wbox_swizzle = [](uint32_t a) { return a ^ (((a >> 7) & kWSwMask) << 4); };
     extern __shared__ __align__(1024) uint8_t smem[];
     // bounded pipeline wait reporting to the library's status word
     auto mbar_wait = [&](uint32_t bar, uint32_t parity, volatile int* abort) {
@@ -570,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 for (int j = 0; j < SUB; ++j) {
                     uint4 raw[4];
                     const uint32_t wsrc = st + w_off + r * (SUB * kRowB) + j * kRowB + h * (kRowB / 2);
-                    raw[0] = lds128u(wsrc);
-                    if constexpr (WF == WF_INT8 || WF == WF_CODES8) raw[1] = lds128u(wsrc + 16);
+                    raw[0] = lds128u(wbox_swizzle(wsrc));
+                    if constexpr (WF == WF_INT8 || WF == WF_CODES8) raw[1] = lds128u(wbox_swizzle(wsrc + 16));
                     float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and sub-stage
                     if constexpr (G::kTable) {
                         // K-block of the sub-stage in the box (the box starts at the stage's
@@ -827,9 +833,11 @@ inline cudaError_t make_wmap(CUtensorMap* map, const void* Bp, int wf, bool bf16
         const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
         const cuuint32_t box[2] = {(cuuint32_t)box_bytes, (cuuint32_t)kBM};
         const cuuint32_t estr[2] = {1, 1};
+        // swizzle span = the box row (32, 64 or 128 bytes); the kernel reads with the same XOR
+        const CUtensorMapSwizzle sw = box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                      : (box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
         r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Bp), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
