@@ -101,12 +101,38 @@ __device__ __forceinline__ void quantize8(const float (&v)[8], float s, float rc
     }
 }
 
-// One block per row. The row is read once: each thread keeps up to kCache chunks of 8 values in
-// registers between the max pass and the quantize pass (K <= 4096); longer rows re-read the rest.
+// One block per row. The row is read once: each thread keeps up to kCache chunks of 8 values as
+// raw bits in registers between the max pass and the quantize pass (K <= 4096), all requested
+// before the first is used; longer rows re-read the rest. Raw 16-bit words keep the register
+// count at 40 for 16-bit activations (6 blocks per SM; measured at 2048 x 4096 bf16: 9.4 us, against
+// 9.6 us with float values cached at 48 registers and 9.7 us when held to 32 registers).
+template <int ADT>
+struct Raw8 {   // 8 activations as stored
+    static constexpr int kWords = ADT == DT_F32 ? 8 : 4;
+    uint32_t w[kWords];
+    __device__ __forceinline__ void load(const void* A, size_t i) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(A) + i * (ADT == DT_F32 ? 4 : 2));
+        const uint4 x = __ldcs(p);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+        if constexpr (ADT == DT_F32) {
+            const uint4 y = __ldcs(p + 1);
+            w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
+        }
+    }
+    __device__ __forceinline__ void values(float (&v)[8]) const {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if constexpr (ADT == DT_F32) v[j] = __uint_as_float(w[j]);
+            else if constexpr (ADT == DT_BF16) v[j] = __uint_as_float((j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16));
+            else v[j] = __half2float(__ushort_as_half((unsigned short)(w[j >> 1] >> (16 * (j & 1)))));
+        }
+    }
+};
+
 template <int ADT, bool H16, bool Q8>
-__global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* __restrict__ A,
-                                                             int8_t* __restrict__ qa, __half* __restrict__ qa16,
-                                                             float* __restrict__ as, int32_t* __restrict__ rowsum) {
+__global__ void __launch_bounds__(kThreads, ADT == DT_F32 ? 4 : 6) act_quant_kernel(
+    int K, const void* __restrict__ A, int8_t* __restrict__ qa, __half* __restrict__ qa16, float* __restrict__ as,
+    int32_t* __restrict__ rowsum) {
     constexpr int kCache = 2;
     __shared__ float s_max[kThreads / 32];
     __shared__ int s_sum[kThreads / 32];
@@ -114,22 +140,29 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t row = (size_t)m * K;
 
-    float v[kCache][8];
-    float amax = 0.f;
+    Raw8<ADT> c[kCache];
 #pragma unroll
     for (int i = 0; i < kCache; ++i) {
         const int k = (threadIdx.x + i * kThreads) * 8;
-        if (k < K) {
-            load8<ADT>(A, row + k, v[i]);
+        if (k < K) c[i].load(A, row + k);
+    }
+    float amax = 0.f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[i][j]));
+    for (int i = 0; i < kCache; ++i) {
+        if ((threadIdx.x + i * kThreads) * 8 < K) {
+            float v[8];
+            c[i].values(v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
         }
     }
     for (int k = (threadIdx.x + kCache * kThreads) * 8; k < K; k += kThreads * 8) {
-        float w[8];
-        load8<ADT>(A, row + k, w);
+        Raw8<ADT> x;
+        float v[8];
+        x.load(A, row + k);
+        x.values(v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(w[j]));
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -144,22 +177,28 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(int K, const void* 
     const float rcp = (s != 0.f && !exact) ? __frcp_rn(s) : 0.f;
 
     int sum = 0;
-    auto emit = [&](int k, const float (&w)[8]) {
+    auto emit = [&](int k, const float (&v)[8]) {
         uint4 h16;
         uint2 q8;
-        quantize8<H16, Q8>(w, s, rcp, exact, sum, h16, q8);
+        quantize8<H16, Q8>(v, s, rcp, exact, sum, h16, q8);
         if constexpr (H16) *reinterpret_cast<uint4*>(qa16 + row + k) = h16;
         if constexpr (Q8) *reinterpret_cast<uint2*>(qa + row + k) = q8;
     };
 #pragma unroll
     for (int i = 0; i < kCache; ++i) {
         const int k = (threadIdx.x + i * kThreads) * 8;
-        if (k < K) emit(k, v[i]);
+        if (k < K) {
+            float v[8];
+            c[i].values(v);
+            emit(k, v);
+        }
     }
     for (int k = (threadIdx.x + kCache * kThreads) * 8; k < K; k += kThreads * 8) {
-        float w[8];
-        load8<ADT>(A, row + k, w);
-        emit(k, w);
+        Raw8<ADT> x;
+        float v[8];
+        x.load(A, row + k);
+        x.values(v);
+        emit(k, v);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
