@@ -433,6 +433,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
     static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
 
+    // Stage i of this split (ks0 + i) into ring slot s: the SUB activation boxes, the weight box
+    // and (formats with a table) the {offset, scale} entries of the stage's K-blocks, all
+    // completing full_x(s). Issued by thread 0 (the TMA producer's lane) only.
+    const uint32_t stage_tx = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
+    auto issue_stage = [&](int i, int s) {
+        const int ks = ks0 + i;
+        const uint32_t st = st_s + (uint32_t)s * SB;
+        mbar_expect_tx(full_x(s), stage_tx);
+#pragma unroll
+        for (int j = 0; j < SUB; ++j) tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
+        // weight box: x in bytes for the packed formats, in elements for float mode
+        tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
+        if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
+                                   // (the box holds tblocks K-blocks, the stage's first one first)
+            tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_x(s), 1);
@@ -447,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         ptx::prefetch_tmap(&maps.a);
         ptx::prefetch_tmap(&maps.w);
         if constexpr (G::kTable) ptx::prefetch_tmap(&maps.t);
+        // the first stage leaves before the block barrier and the tensor-memory allocation (its
+        // ring slot starts free)
+        if (nks > 0) issue_stage(0, 0);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -462,22 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- TMA producer: per stage the SUB activation boxes, the weight box and
         // (formats with a table) the {offset, scale} entries of the stage's K-blocks
         if (lane == 0) {
-            const uint32_t bytes = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
-            int issued = 0, s = 0;
-            uint32_t ph = 0;
-            for (int i = 0; i < nks; ++i) {
-                const int ks = ks0 + i;
+            // stage 0 went out before the block barrier
+            int issued = nks > 0 ? 1 : 0, s = 1 % S;
+            uint32_t ph = S == 1 ? 1u : 0u;
+            for (int i = 1; i < nks; ++i) {
                 if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                mbar_expect_tx(full_x(s), bytes);
-#pragma unroll
-                for (int j = 0; j < SUB; ++j)
-                    tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
-                // weight box: x in bytes for the packed formats, in elements for float mode
-                tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
-                if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
-                                           // (the box holds tblocks K-blocks, the stage's first one first)
-                    tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
+                issue_stage(i, s);
                 issued = i + 1;
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
