@@ -49,9 +49,15 @@ namespace pf {
 constexpr int kBM = 128;              // output channels per tile (MMA M)
 constexpr int kBK = 64;               // K per pipeline stage
 constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
-constexpr int kWarps = 10;            // 0: TMA, 1: MMA + TMEM, 2..9: dequant + epilogue
+// warps: 0 TMA (activation boxes), 1 MMA + TMEM, 2..9 dequant + epilogue, 10 TMA (weight and
+// table boxes). Two producer lanes in different warps issue a stage's copies side by side: one
+// lane issuing all of a stage's copies paced the Int4 prefill at ~440 ns per stage, above the
+// MMA's ~320 ns (measured with per-stage timestamps).
+constexpr int kWarps = 11;
 constexpr int kThreads = kWarps * 32;
-constexpr int kEpiThreads = (kWarps - 2) * 32;   // dequant + epilogue threads
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;   // dequant + epilogue threads (warps 2 .. 9)
+constexpr int kWProdWarp = 2 + kEpiWarps;     // the weight / table producer warp
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;            // accumulator columns [0, BN); the A stages follow
 
@@ -433,21 +439,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
     static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
 
-    // Stage i of this split (ks0 + i) into ring slot s: the SUB activation boxes, the weight box
-    // and (formats with a table) the {offset, scale} entries of the stage's K-blocks, all
-    // completing full_x(s). Issued by thread 0 (the TMA producer's lane) only.
+    // Stage i of this split (ks0 + i) into ring slot s, all copies completing full_x(s): the SUB
+    // activation boxes with the expected bytes of the whole stage (issue_act, warp 0), and the
+    // weight box and (formats with a table) the {offset, scale} entries of the stage's K-blocks
+    // (issue_wt, warp kWProdWarp). A copy may complete before the expect_tx arrival; the phase
+    // still waits for that arrival.
     const uint32_t stage_tx = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
-    auto issue_stage = [&](int i, int s) {
+    auto issue_act = [&](int i, int s) {
         const int ks = ks0 + i;
         const uint32_t st = st_s + (uint32_t)s * SB;
         mbar_expect_tx(full_x(s), stage_tx);
 #pragma unroll
         for (int j = 0; j < SUB; ++j) tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
+    };
+    auto issue_wt = [&](int i, int s) {
+        const int ks = ks0 + i;
+        const uint32_t st = st_s + (uint32_t)s * SB;
         // weight box: x in bytes for the packed formats, in elements for float mode
         tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
         if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
                                    // (the box holds tblocks K-blocks, the stage's first one first)
             tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
+    };
+    // A producer lane's loop over stages 1 .. nks - 1 (stage 0 leaves before the block barrier):
+    // each waits for its slot, then `issue`; after an abort, the copies it issued land before the
+    // block exits. Returns the stages issued.
+    auto produce = [&](auto&& issue) {
+        int issued = nks > 0 ? 1 : 0, s = 1 % S;
+        uint32_t ph = S == 1 ? 1u : 0u;
+        for (int i = 1; i < nks; ++i) {
+            if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+            issue(i, s);
+            issued = i + 1;
+            if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        if (*abort_flag) {
+            for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
+                volatile int never = 0;
+                ptx::mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never, p.status);
+            }
+        }
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -465,7 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if constexpr (G::kTable) ptx::prefetch_tmap(&maps.t);
         // the first stage leaves before the block barrier and the tensor-memory allocation (its
         // ring slot starts free)
-        if (nks > 0) issue_stage(0, 0);
+        if (nks > 0) {
+            issue_act(0, 0);
+            issue_wt(0, 0);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -477,25 +511,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
     const uint32_t a_col = tmem + (uint32_t)BN;        // A stages follow the BN accumulator columns
 
-    if (warp == 0) {
-        // ---------------- TMA producer: per stage the SUB activation boxes, the weight box and
-        // (formats with a table) the {offset, scale} entries of the stage's K-blocks
+    if (warp == kWProdWarp) {
+        // ---------------- TMA producer of the weight and table boxes
+        if (lane == 0) produce(issue_wt);
+    } else if (warp == 0) {
+        // ---------------- TMA producer of the activation boxes (and the residual tile)
         if (lane == 0) {
-            // stage 0 went out before the block barrier
-            int issued = nks > 0 ? 1 : 0, s = 1 % S;
-            uint32_t ph = S == 1 ? 1u : 0u;
-            for (int i = 1; i < nks; ++i) {
-                if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-                issue_stage(i, s);
-                issued = i + 1;
-                if (++s == S) { s = 0; ph ^= 1u; }
-            }
-            if (*abort_flag) {   // let the copies already issued land before the block exits
-                for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
-                    volatile int never = 0;
-                    ptx::mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never, p.status);
-                }
-            } else if (EPI != EPI_ACC && p.r_tma) {
+            produce(issue_act);
+            if (!*abort_flag && EPI != EPI_ACC && p.r_tma) {
                 // The residual tile lands where the output tile is staged, [0, kTileBytes): as
                 // soon as the MMAs of the last use of every ring slot under that range are done
                 // (a few stages before the end of K), one TMA load brings it in, so its latency
