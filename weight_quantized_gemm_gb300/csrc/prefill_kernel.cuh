@@ -50,14 +50,16 @@ constexpr int kBM = 128;              // output channels per tile (MMA M)
 constexpr int kBK = 64;               // K per pipeline stage
 constexpr int kMaxBN = 256;           // rows of A per tile (MMA N), a multiple of 64
 // warps: 0 TMA (activation boxes), 1 MMA + TMEM, 2..9 dequant + epilogue, 10 TMA (weight and
-// table boxes). Two producer lanes in different warps issue a stage's copies side by side: one
-// lane issuing all of a stage's copies paced the Int4 prefill at ~440 ns per stage, above the
-// MMA's ~320 ns (measured with per-stage timestamps).
-constexpr int kWarps = 11;
+// table boxes), 11 the output tiles' TMA stores and the residual tiles' loads. Two producer lanes
+// in different warps issue a stage's copies side by side: one lane issuing all of a stage's copies
+// paced the Int4 prefill at ~440 ns per stage, above the MMA's ~320 ns (measured with per-stage
+// timestamps).
+constexpr int kWarps = 12;
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;   // dequant + epilogue threads (warps 2 .. 9)
 constexpr int kWProdWarp = 2 + kEpiWarps;     // the weight / table producer warp
+constexpr int kStoreWarp = kWProdWarp + 1;    // the store warp
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;            // accumulator columns [0, BN); the A stages follow
 
@@ -346,9 +348,10 @@ struct Geo {
 };
 // The kernel's shape for tile height BN, fixed at compile time: two 64-wide sub-stages per stage
 // (half the barrier rounds per unit of K) where the ring still holds at least kMinSub2Stages of
-// them -- small tiles, whose stages are short and whose per-round costs dominate; large tiles keep
-// 64-wide stages, whose finer-grained ring refills sooner.
-constexpr int kMinSub2Stages = 5;
+// them. The MMA issuer's per-stage work (barrier wait, commit) leaves the tensor pipe idle for a
+// moment each stage, so fewer, larger stages keep it busier (measured on 256-row tiles: three
+// 128-wide stages ran the W4A8 and Int4 prefill GEMMs 4-9% faster than six 64-wide ones).
+constexpr int kMinSub2Stages = 3;
 template <int WF, bool BF, int BN>
 struct Plan {
     static constexpr int kSub = (WF != WF_FLOAT && Geo<WF, BF, 2>::stages(BN) >= kMinSub2Stages) ? 2 : 1;
@@ -361,6 +364,25 @@ struct Plan {
     static_assert(BN + kStages * G::kCols <= kTmemCols, "accumulator and A stages fit in TMEM");
     static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned (128-byte swizzle atoms)");
 };
+// The staged output tile [BN rows][128 channels] in C's type (int32 accumulators: 4 bytes) takes
+// kSlots consecutive ring slots. Persistent form, where a tile's staging leaves the ring at least
+// one slot for the next tile (2 kSlots - 1 <= stages: the reserved slots may have to skip the
+// ring's last ones to stay contiguous): at most one block per SM runs through a sequence of tiles.
+// After a tile's last stage the pipeline takes kSlots "staging positions" (plus skipped ones) in
+// ring order: the producers put no copies there until the tile's TMA store has read them, while
+// they already fill the other slots with the next tile's stages, so the store drains and the next
+// tile's loads, dequantization and MMAs start behind the epilogue, and the block's setup (barriers,
+// tensor memory, the first copies) is paid once. Otherwise (float32 or int32 tiles of 256 rows)
+// the tile is staged over the first slots, idle after the tile's last MMA, and the grid holds one
+// block per tile.
+template <int WF, bool BF, int EPI, int CDT, int BN>
+struct Tiling {
+    using P = Plan<WF, BF, BN>;
+    static constexpr int kTileBytes = BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
+    static constexpr int kSlots = (kTileBytes + P::kStageBytes - 1) / P::kStageBytes;
+    static constexpr bool kPersistent = 2 * kSlots - 1 <= P::kStages;
+    static_assert(kSlots <= P::kStages, "the staged tile fits in the ring");
+};
 struct Maps {                 // the kernel's tensor maps
     CUtensorMap a;            // activations
     CUtensorMap w;            // packed weights
@@ -369,11 +391,27 @@ struct Maps {                 // the kernel's tensor maps
     CUtensorMap r;            // the epilogue's residual, when Params::r_tma (same layout as c)
 };
 
-// One thread block: output channels [128 x, 128 x + 128) x rows of A [BN y, BN y + BN), and the
-// stages of K-split z (all of K when p.splits == 1).
+// OR of v over the dequant / epilogue warps (named barrier 1): the same answer in every thread.
+__device__ __forceinline__ bool epi_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kEpiThreads)
+        : "memory");
+    return r != 0;
+}
+
+// One thread block runs the output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... (one tile per
+// block unless Tiling::kPersistent): tile t covers output channels [128 x, 128 x + 128) x rows of
+// A [BN y, BN y + BN) (the raster below maps t to x, y) over the stages of K-split z (all of K
+// when p.splits == 1). Every role walks the same sequence of ring positions: per tile its stages,
+// then (persistent form) its staging positions; position g uses ring slot g % S, and every
+// position completes one phase of each of the slot's barriers.
 template <int WF, bool BF, int EPI, int CDT, int BN>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ Maps maps, Params p) {
-    using P = Plan<WF, BF, BN>;
+    using T = Tiling<WF, BF, EPI, CDT, BN>;
+    using P = typename T::P;
     using G = typename P::G;
     constexpr int SUB = P::kSub, S = P::kStages;
     constexpr uint32_t SB = P::kStageBytes;
@@ -395,35 +433,38 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr uint32_t kABytes = (uint32_t)BN * kBK * 2;   // one activation box
     constexpr uint32_t w_off = SUB * kABytes, t_off = w_off + G::kWBytes;
     // Raster. Weights larger than the L2 share: groups of group_n channel tiles with the row tiles
-    // fastest inside a group, so the blocks running at the same time share each weight tile (read
+    // fastest inside a group, so the tiles running at the same time share each weight tile (read
     // from HBM once) and re-read only the activations, which stay in L2. Otherwise channel tiles
     // fastest (group_n == 0): the weights stay in L2 and each activation tile is read by a run of
-    // consecutive blocks.
-    int n_idx, m_idx;
-    if (p.group_n > 0) {
-        const int per_group = p.group_n * p.m_tiles;
-        const int grp = (int)blockIdx.x / per_group, in_grp = (int)blockIdx.x - grp * per_group;
-        // (the last group may hold fewer channel tiles; the grid covers exactly n_tiles x m_tiles)
-        n_idx = grp * p.group_n + in_grp / p.m_tiles;
-        m_idx = in_grp % p.m_tiles;
-    } else {
-        const int n_tiles = (p.N + kBM - 1) / kBM;
-        n_idx = (int)blockIdx.x % n_tiles;
-        m_idx = (int)blockIdx.x / n_tiles;
-    }
-    const int n_tile = n_idx * kBM, m_tile = m_idx * BN;
+    // consecutive tiles.
+    const int n_tiles = (p.N + kBM - 1) / kBM;
+    const int total = n_tiles * p.m_tiles;
+    auto tile_of = [&](int t) {   // {channel tile, row tile} of tile t
+        if (p.group_n > 0) {
+            const int per_group = p.group_n * p.m_tiles;
+            const int grp = t / per_group, in_grp = t - grp * per_group;
+            // (the last group may hold fewer channel tiles; the tiles cover exactly n_tiles x m_tiles)
+            return make_int2(grp * p.group_n + in_grp / p.m_tiles, in_grp % p.m_tiles);
+        }
+        return make_int2(t % n_tiles, t / n_tiles);
+    };
     const int nsub = p.K / kBK;                        // 64-wide sub-stages of K
     const int nst = (nsub + SUB - 1) / SUB;            // stages (the last may be half past K: reads 0)
-    // split z covers stages [ks0, ks0 + nks); the ring counts stages from 0 within the split
+    // split z covers stages [ks0, ks0 + nks) of every tile
     const int ks0 = (int)((long long)nst * blockIdx.z / p.splits);
     const int nks = (int)((long long)nst * (blockIdx.z + 1) / p.splits) - ks0;
     const int bpb = p.block / kBK;                     // sub-stages per table block
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRing);
     // bars: full[S] (the stage's boxes landed) | full_a[S] (TMEM A stage written) |
-    //       empty[S] (MMAs of the stage done) | acc_full
-    // ... | res_full (the residual tile landed, Params::r_tma) | stall (Params::stall: never arrived at)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 3);
+    //       empty[S] (MMAs of the stage done) | acc_full (the tile's MMAs done) |
+    //       res_full (the residual tile landed, Params::r_tma) | stall (Params::stall: never
+    //       arrived at) | acc_empty (the epilogue warps have read the accumulator) |
+    //       staged (the output tile is staged) | taken (the store warp has taken it)
+    // A barrier's waiter must never fall two phases behind it (a parity wait would then pass on
+    // the wrong phase): every wait below is on a phase that cannot complete twice without the
+    // waiter's own progress.
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 6);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
     float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
@@ -434,61 +475,128 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t acc_full = smem_u32(bars + 3 * kMaxStages);
     const uint32_t res_full = smem_u32(bars + 3 * kMaxStages + 1);
     const uint32_t stall_bar = smem_u32(bars + 3 * kMaxStages + 2);
-    static_assert((3 * kMaxStages + 3) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
-    // bytes of the staged output tile [BN rows][128 channels], where the residual tile also lands
-    constexpr uint32_t kTileBytes = (uint32_t)BN * kBM * ((EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2);
-    static_assert(kTileBytes <= (uint32_t)kRing, "the staged tile fits in the ring");
+    const uint32_t acc_empty = smem_u32(bars + 3 * kMaxStages + 3);
+    const uint32_t staged = smem_u32(bars + 3 * kMaxStages + 4);
+    const uint32_t taken = smem_u32(bars + 3 * kMaxStages + 5);
+    static_assert((3 * kMaxStages + 6) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
+    constexpr uint32_t kTileBytes = (uint32_t)T::kTileBytes;
+    // Staging positions after a tile whose stages end at position g_end: returns their count and
+    // sets *slot to the first of the kSlots contiguous slots where the tile is staged (the
+    // positions before it, if any, skip the ring's last slots). Not persistent: none; the tile is
+    // staged from slot 0.
+    auto staging_of = [](int g_end, int* slot) {
+        if constexpr (!T::kPersistent) {
+            *slot = 0;
+            return 0;
+        } else {
+            const int a = g_end % S;
+            *slot = a + T::kSlots > S ? 0 : a;
+            return a + T::kSlots > S ? S - a + T::kSlots : T::kSlots;
+        }
+    };
 
-    // Stage i of this split (ks0 + i) into ring slot s, all copies completing full_x(s): the SUB
-    // activation boxes with the expected bytes of the whole stage (issue_act, warp 0), and the
-    // weight box and (formats with a table) the {offset, scale} entries of the stage's K-blocks
-    // (issue_wt, warp kWProdWarp). A copy may complete before the expect_tx arrival; the phase
-    // still waits for that arrival.
+    // Stage i of this split (ks0 + i) of tile tc into ring slot s, all copies completing
+    // full_x(s): the SUB activation boxes with the expected bytes of the whole stage (issue_act,
+    // warp 0), and the weight box and (formats with a table) the {offset, scale} entries of the
+    // stage's K-blocks (issue_wt, warp kWProdWarp). A copy may complete before the expect_tx
+    // arrival; the phase still waits for that arrival.
     const uint32_t stage_tx = SUB * kABytes + (uint32_t)G::kWBytes + (G::kTable ? (uint32_t)p.tblocks * 1024u : 0u);
-    auto issue_act = [&](int i, int s) {
+    auto issue_act = [&](int2 tc, int i, int s) {
         const int ks = ks0 + i;
         const uint32_t st = st_s + (uint32_t)s * SB;
         mbar_expect_tx(full_x(s), stage_tx);
 #pragma unroll
-        for (int j = 0; j < SUB; ++j) tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, m_tile, full_x(s));
+        for (int j = 0; j < SUB; ++j) tma_load_2d(st + j * kABytes, &maps.a, (ks * SUB + j) * kBK, tc.y * BN, full_x(s));
     };
-    auto issue_wt = [&](int i, int s) {
+    auto issue_wt = [&](int2 tc, int i, int s) {
         const int ks = ks0 + i;
         const uint32_t st = st_s + (uint32_t)s * SB;
         // weight box: x in bytes for the packed formats, in elements for float mode
-        tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, n_tile, full_x(s));
+        tma_load_2d(st + w_off, &maps.w, WF == WF_FLOAT ? ks * kBK : ks * SUB * kRowB, tc.x * kBM, full_x(s));
         if constexpr (G::kTable)   // 8 groups of 16 channels: x = 32 floats per K-block, y = group
                                    // (the box holds tblocks K-blocks, the stage's first one first)
-            tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), n_tile / 16, full_x(s));
+            tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), tc.x * (kBM / 16), full_x(s));
     };
-    // A producer lane's loop over stages 1 .. nks - 1 (stage 0 leaves before the block barrier):
-    // each waits for its slot, then `issue`; after an abort, the copies it issued land before the
-    // block exits. Returns the stages issued.
-    auto produce = [&](auto&& issue) {
-        int issued = nks > 0 ? 1 : 0, s = 1 % S;
-        uint32_t ph = S == 1 ? 1u : 0u;
-        for (int i = 1; i < nks; ++i) {
-            if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-            issue(i, s);
-            issued = i + 1;
-            if (++s == S) { s = 0; ph ^= 1u; }
+    // A producer lane's walk over the block's ring positions (the first one leaves before the
+    // block barrier): at a stage it waits for the slot's previous use, then `issue`s; at a staging
+    // position the activation producer (act) waits the same way and arrives on full_x without
+    // copies, the weight producer passes. The activation producer also brings in the residual tile
+    // (Params::r_tma) where the tile is staged, as soon as the staging slots' previous uses are
+    // done, so that its latency hides behind the tile's last stages. After an abort, the copies
+    // issued land before the block exits.
+    auto produce = [&](auto&& issue, bool act) {
+        const bool res = act && EPI != EPI_ACC && p.r_tma;
+        int g = 0, s = 0, tj = 0, res_issued = 0;
+        uint32_t ph = 0, real = 0;                     // real: bit s = the last use of slot s had copies
+        bool stop = false;
+        auto load_res = [&](int2 tc, int slot) {
+            mbar_expect_tx(res_full, kTileBytes);
+            ptx::tma_load_3d(st_s + (uint32_t)slot * SB, &maps.r, tc.x * kBM, tc.y * BN, 0, res_full);
+            ++res_issued;
+        };
+        for (int t = blockIdx.x; t < total && !stop; t += gridDim.x, ++tj) {
+            const int2 tc = tile_of(t);
+            int slot;
+            const int np = nks + staging_of(g + nks, &slot);
+            for (int i = 0; i < np; ++i) {
+                if (g > 0 && (i < nks || act)) {
+                    if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    if (i < nks) issue(tc, i, s);
+                    else mbar_arrive(full_x(s));
+                }
+                real = i < nks ? real | (1u << s) : real & ~(1u << s);
+                ++g;
+                if (++s == S) { s = 0; ph ^= 1u; }
+                // the last staging position: every staging slot's previous use is done; the
+                // previous tile's residual has been read (its staged tile was taken)
+                if (res && i == np - 1 && np > nks) {
+                    if (tj > 0 && !mbar_wait(taken, (uint32_t)(tj - 1) & 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    load_res(tc, slot);
+                }
+            }
+        }
+        if constexpr (!T::kPersistent) {
+            // one tile, staged over the first slots: the residual comes in once the last use of
+            // each slot under the staged tile is done
+            if (res && !stop && !*abort_flag && total > (int)blockIdx.x) {
+                bool free = true;
+                for (int sl = 0; sl < T::kSlots && sl < nks && free; ++sl) {
+                    const int last = sl + ((nks - 1 - sl) / S) * S;   // its last use
+                    free = mbar_wait(empty(sl), (uint32_t)(last / S) & 1u, abort_flag);
+                }
+                if (free) load_res(tile_of(blockIdx.x), 0);
+            }
         }
         if (*abort_flag) {
-            for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i) {
+            for (int gg = g - S < 0 ? 0 : g - S; gg < g; ++gg) {
+                if (!act && !((real >> (gg % S)) & 1u)) continue;   // no copies of this lane there
                 volatile int never = 0;
-                ptx::mbar_wait(full_x(i % S), (uint32_t)(i / S) & 1u, &never, p.status);
+                ptx::mbar_wait(full_x(gg % S), (uint32_t)(gg / S) & 1u, &never, p.status);
+            }
+            if (res_issued > 0) {   // a residual tile still in flight
+                volatile int never = 0;
+                ptx::mbar_wait(res_full, (uint32_t)(res_issued - 1) & 1u, &never, p.status);
             }
         }
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_x(s), 1);
-            mbar_init(full_a(s), 8);   // one arrival per dequant warp
-            mbar_init(empty(s), 1);    // one tcgen05.commit per use
+            mbar_init(full_a(s), kEpiWarps);   // one arrival per dequant warp
+            mbar_init(empty(s), 1);            // one tcgen05.commit per use
         }
         mbar_init(acc_full, 1);
         mbar_init(res_full, 1);
         mbar_init(stall_bar, 1);
+        mbar_init(acc_empty, kEpiWarps);
+        mbar_init(staged, 1);
+        mbar_init(taken, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
@@ -496,9 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if constexpr (G::kTable) ptx::prefetch_tmap(&maps.t);
         // the first stage leaves before the block barrier and the tensor-memory allocation (its
         // ring slot starts free)
-        if (nks > 0) {
-            issue_act(0, 0);
-            issue_wt(0, 0);
+        if (nks > 0 && (int)blockIdx.x < total) {
+            const int2 tc = tile_of(blockIdx.x);
+            issue_act(tc, 0, 0);
+            issue_wt(tc, 0, 0);
         }
     }
     if (warp == 1) {
@@ -513,307 +622,359 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     if (warp == kWProdWarp) {
         // ---------------- TMA producer of the weight and table boxes
-        if (lane == 0) produce(issue_wt);
+        if (lane == 0) produce(issue_wt, false);
     } else if (warp == 0) {
-        // ---------------- TMA producer of the activation boxes (and the residual tile)
+        // ---------------- TMA producer of the activation boxes
+        if (lane == 0) produce(issue_act, true);
+    } else if (warp == kStoreWarp) {
+        // ---------------- the staged tiles out (one TMA store each), then their staging positions
+        // released to the producers
         if (lane == 0) {
-            produce(issue_act);
-            if (!*abort_flag && EPI != EPI_ACC && p.r_tma) {
-                // The residual tile lands where the output tile is staged, [0, kTileBytes): as
-                // soon as the MMAs of the last use of every ring slot under that range are done
-                // (a few stages before the end of K), one TMA load brings it in, so its latency
-                // hides behind the last stages.
-                bool free = true;
-                for (int sl = 0; sl < S && (uint32_t)sl * SB < kTileBytes && free; ++sl) {
-                    if (sl >= nks) break;                              // never used
-                    const int last = sl + ((nks - 1 - sl) / S) * S;    // its last use
-                    free = mbar_wait(empty(sl), (uint32_t)(last / S) & 1u, abort_flag);
+            int g = 0;
+            for (int t = blockIdx.x, tj = 0; t < total; t += gridDim.x, ++tj) {
+                int slot;
+                const int g_end = g + nks;
+                g = g_end + staging_of(g_end, &slot);
+                if (!mbar_wait(staged, (uint32_t)tj & 1u, abort_flag)) break;
+                mbar_arrive(taken);
+                if (p.c_tma) {
+                    // rows and channels past the end are not written
+                    const int2 tc = tile_of(t);
+                    const uint32_t stile = st_s + (uint32_t)slot * SB;
+                    if (EPI == EPI_ACC && p.acc_add)
+                        ptx::tma_reduce_add_3d(&maps.c, tc.x * kBM, tc.y * BN, 0, stile);
+                    else
+                        ptx::tma_store_3d(&maps.c, tc.x * kBM, tc.y * BN, blockIdx.z, stile);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read();
                 }
-                if (free) {
-                    mbar_expect_tx(res_full, kTileBytes);
-                    ptx::tma_load_3d(st_s, &maps.r, n_tile, m_tile, 0, res_full);
-                    volatile int never = 0;   // stay until it has landed (the epilogue reads it)
-                    ptx::mbar_wait(res_full, 0u, &never, p.status);
-                }
+                for (int k = g_end; k < g; ++k) mbar_arrive(empty(k % S));   // the staging positions
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer. tcgen05.mma issue stalls while the tensor pipe's queue is
+        // full, so the instructions between one stage's last MMA and the next stage's first one
+        // leave the pipe idle: the next stage's barrier is tested before the stage's last MMA (with
+        // MMAs still queued) and, when already complete, not waited for again.
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(BF, BN, kBM);
-            int s = 0;
+            int g = 0, s = 0, commits = 0;
             uint32_t ph = 0;
+            bool stop = false;
             if (p.stall) mbar_wait(stall_bar, 0u, abort_flag);   // diagnostic: runs out, raises the abort flag
-            for (int i = 0; i < nks; ++i) {
-                // With dequant warps, full_a is enough: every dequant warp waited for the stage's
-                // TMA barrier (activations included) before it arrived on full_a, so acquiring
-                // full_a orders the landed boxes before these MMAs. One wait fewer per stage on
-                // this thread, which paces the tensor pipe (measured: W4A8 4.5% faster).
-                if constexpr (kDequant) {
-                    if (!mbar_wait(full_a(s), ph, abort_flag)) break;
-                } else {
-                    if (!mbar_wait(full_x(s), ph, abort_flag)) break;
-                }
-                tc_fence_after();
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                const uint32_t as = a_col + (uint32_t)(s * G::kCols);
+            // With dequant warps the MMAs wait on full_a only: every dequant warp waited for the
+            // stage's TMA barrier (activations included) before it arrived on full_a, so acquiring
+            // full_a orders the landed boxes before these MMAs.
+            auto ready_bar = [&](int sl) { return kDequant ? full_a(sl) : full_x(sl); };
+            for (int t = blockIdx.x, tj = 0; t < total && !stop && !*abort_flag; t += gridDim.x, ++tj) {
+                int slot, skip = staging_of(g + nks, &slot);   // the tile's staging positions: no MMAs
+                // the accumulator is free once the epilogue warps have read the previous tile
+                if (tj > 0 && !mbar_wait(acc_empty, (uint32_t)(tj - 1) & 1u, abort_flag)) break;
+                bool ready = false;                            // stage i's barrier was seen complete
+#pragma unroll 2
+                for (int i = 0; i < nks; ++i) {
+                    if (!ready && !mbar_wait(ready_bar(s), ph, abort_flag)) { stop = true; break; }
+                    tc_fence_after();
+                    const uint32_t st = st_s + (uint32_t)s * SB;
+                    const uint32_t as = a_col + (uint32_t)(s * G::kCols);
 #pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    const uint64_t bdesc = sw128_desc(st + j * kABytes);
+                    for (int j = 0; j < SUB; ++j) {
+                        const uint64_t bdesc = sw128_desc(st + j * kABytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t acc = (i | j | kk) != 0;
-                        if constexpr (kDequant) {
-                            mma_ts(tmem, as + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, acc);
-                            if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
-                                mma_ts(tmem, as + kLo + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, 1u);
-                        } else {
-                            const uint64_t adesc = sw128_desc(st + w_off);
-                            mma_ss(tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc, acc);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            if (j == SUB - 1 && kk == kBK / 16 - 1)   // before the stage's last MMA
+                                ready = i + 1 < nks && ptx::mbar_try_wait(ready_bar(s + 1 == S ? 0 : s + 1),
+                                                                          s + 1 == S ? ph ^ 1u : ph);
+                            const uint32_t acc = (i | j | kk) != 0;   // the tile's first MMA overwrites
+                            if constexpr (kDequant) {
+                                mma_ts(tmem, as + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, acc);
+                                if constexpr (Split<WF, BF>::kOn)   // the low parts of the same weights
+                                    mma_ts(tmem, as + kLo + 32 * j + kk * 8, bdesc + (uint64_t)(2 * kk), idesc, 1u);
+                            } else {
+                                const uint64_t adesc = sw128_desc(st + w_off);
+                                mma_ss(tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc, acc);
+                            }
                         }
                     }
+                    mma_commit(empty(s));
+                    ++g;
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
-                mma_commit(empty(s));
-                if (++s == S) { s = 0; ph ^= 1u; }
+                mma_commit(acc_full);   // also after an abort: completes once every issued MMA has finished
+                ++commits;
+                for (; skip > 0; --skip) {
+                    ++g;
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
             }
-            mma_commit(acc_full);   // also on abort: completes once every issued MMA has finished
+            if (*abort_flag && commits > 0) {
+                // the MMAs already issued finish before their tensor memory is released
+                volatile int never = 0;
+                ptx::mbar_wait(acc_full, (uint32_t)(commits - 1) & 1u, &never, p.status);
+            }
         }
     } else {
-        if constexpr (EPI == EPI_W4A8) {
-            // the row factors, once per tile, while the first stages are in flight
-            for (int i = threadIdx.x - 64; i < BN; i += kEpiThreads) {
-                const int m = min(m_tile + i, p.M - 1);
-                const float as = p.a_scale ? __ldg(p.a_scale + m) : 1.f;
-                const float rs = p.rowsum ? (float)__ldg(p.rowsum + m) : __ldg(p.rowsum_f + m);
-                rowf[i] = make_float2(as, as * rs);
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-        }
         // ---------------- dequant warps (8): TMEM lane quarter q = warp % 4, K half h of each
-        // 64-wide sub-stage
+        // 64-wide sub-stage; after a tile's last stage, its epilogue
         const int q = warp & 3, h = (warp - 2) >> 2;
         const int r = 32 * q + lane;                 // row inside the tile
-        const int row = n_tile + r;
-        const int rc = row < p.N ? row : p.N - 1;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        if constexpr (kDequant) {
-            int s = 0;
-            uint32_t ph = 0;
-            int pos = (ks0 * SUB) % bpb;             // first sub-stage of the stage, within its K-block
-            for (int i = 0; i < nks; ++i) {
-                if (!mbar_wait(full_x(s), ph, abort_flag)) break;
-                const uint32_t st = st_s + (uint32_t)s * SB;
-                uint32_t out[SUB][16], rest[SUB][16];
-#pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    uint4 raw[4];
-                    const uint32_t wsrc = st + w_off + r * (SUB * kRowB) + j * kRowB + h * (kRowB / 2);
-                    raw[0] = lds128u(wbox_swizzle(wsrc));
-                    if constexpr (WF == WF_INT8 || WF == WF_CODES8) raw[1] = lds128u(wbox_swizzle(wsrc + 16));
-                    float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and sub-stage
-                    if constexpr (G::kTable) {
-                        // K-block of the sub-stage in the box (the box starts at the stage's
-                        // first block); a sub-stage past K (its weights and activations read 0)
-                        // keeps the last block of the box
-                        const int d = (j == 0 || pos + j < bpb) ? 0 : min(1, p.tblocks - 1);
-                        e = lds64f(st + t_off + (r >> 4) * (p.tblocks * 128) + d * 128 + (r & 15) * 8);
-                    }
-                    convert32<WF, BF>(raw, e.y, e.x, out[j], rest[j]);
-                }
-                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t dst = a_col + lane_base + (uint32_t)(s * G::kCols) + 16 * h;
-#pragma unroll
-                for (int j = 0; j < SUB; ++j) {
-                    tmem_st16(dst + 32 * j, out[j]);
-                    if constexpr (Split<WF, BF>::kOn) tmem_st16(dst + kLo + 32 * j, rest[j]);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full_a(s));
-                if (++s == S) { s = 0; ph ^= 1u; }
-                if (SUB > 1 || bpb > 1) {
-                    pos += SUB;
-                    while (pos >= bpb) pos -= bpb;
-                }
-            }
-        }
-        // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
-        // The tile is written transposed into the (now idle) stage buffers as [m][128 n] and then
-        // copied out row by row with 16-byte stores.
-        const bool ok = mbar_wait(acc_full, 0u, abort_flag) && !*abort_flag;
-        tc_fence_after();
         constexpr int kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4 : 2;
-        uint8_t* tile = smem;
-        if (ok) {
-            float ws = 0.f, wo = 0.f;
+        int g = 0, s = 0;
+        uint32_t ph = 0;
+        // W4A8: per row m of a tile {as[m], as[m] * rowsum[m]} (row ri = this thread's row, BN <= 256)
+        const int ri = threadIdx.x - 64;
+        auto row_factors = [&](int m_tile) {
+            const int m = min(m_tile + ri, p.M - 1);
+            const float as = p.a_scale ? __ldg(p.a_scale + m) : 1.f;
+            const float rs = p.rowsum ? (float)__ldg(p.rowsum + m) : __ldg(p.rowsum_f + m);
+            return make_float2(as, as * rs);
+        };
+        for (int t = blockIdx.x, tj = 0; t < total; t += gridDim.x, ++tj) {
+            const int2 tc = tile_of(t);
+            const int n_idx = tc.x, n_tile = tc.x * kBM, m_tile = tc.y * BN;
+            int slot;
+            const int nstg = staging_of(g + nks, &slot);
+            uint8_t* const tile = smem + (size_t)slot * SB;   // where the tile is staged
+            const int row = n_tile + r;
+            const int rc = row < p.N ? row : p.N - 1;
             if constexpr (EPI == EPI_W4A8) {
-                if constexpr (G::kTable) {   // block-quantized W4A8 weights: dequantized per block already
-                    ws = 1.f;
-                    wo = 0.f;
-                } else {                     // raw codes: the per-channel {offset, scale} here
-                    const float2 t = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
-                    wo = t.x;
-                    ws = t.y;
+                // the first tile's row factors while its first stages are in flight (later tiles'
+                // were stored after the previous epilogue's barrier)
+                if (tj == 0 && ri < BN) rowf[ri] = row_factors(m_tile);
+                asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
+            }
+            if constexpr (kDequant) {
+                int pos = (ks0 * SUB) % bpb;         // the first stage's first sub-stage in its K-block
+                for (int i = 0; i < nks; ++i) {
+                    if (!mbar_wait(full_x(s), ph, abort_flag)) break;
+                    const uint32_t st = st_s + (uint32_t)s * SB;
+                    uint32_t out[SUB][16], rest[SUB][16];
+#pragma unroll
+                    for (int j = 0; j < SUB; ++j) {
+                        uint4 raw[4];
+                        const uint32_t wsrc = st + w_off + r * (SUB * kRowB) + j * kRowB + h * (kRowB / 2);
+                        raw[0] = lds128u(wbox_swizzle(wsrc));
+                        if constexpr (WF == WF_INT8 || WF == WF_CODES8) raw[1] = lds128u(wbox_swizzle(wsrc + 16));
+                        float2 e = make_float2(0.f, 1.f);   // {offset, scale} of this row and sub-stage
+                        if constexpr (G::kTable) {
+                            // K-block of the sub-stage in the box (the box starts at the stage's
+                            // first block); a sub-stage past K (its weights and activations read 0)
+                            // keeps the last block of the box
+                            const int d = (j == 0 || pos + j < bpb) ? 0 : min(1, p.tblocks - 1);
+                            e = lds64f(st + t_off + (r >> 4) * (p.tblocks * 128) + d * 128 + (r & 15) * 8);
+                        }
+                        convert32<WF, BF>(raw, e.y, e.x, out[j], rest[j]);
+                    }
+                    if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t dst = a_col + lane_base + (uint32_t)(s * G::kCols) + 16 * h;
+#pragma unroll
+                    for (int j = 0; j < SUB; ++j) {
+                        tmem_st16(dst + 32 * j, out[j]);
+                        if constexpr (Split<WF, BF>::kOn) tmem_st16(dst + kLo + 32 * j, rest[j]);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_a(s));
+                    ++g;
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                    if (SUB > 1 || bpb > 1) {
+                        pos += SUB;
+                        while (pos >= bpb) pos -= bpb;
+                    }
+                }
+            } else {
+                for (int i = 0; i < nks; ++i) {   // the MMA reads the weights from shared memory
+                    ++g;
+                    if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
-            // The fused epilogue: this thread's channel bias once, and per 32-column chunk the 32
-            // residual values (32 independent loads, one 64-byte segment of a residual row per
-            // warp each) before any of them is used; the activation is chosen once per chunk.
+            // The tile's staging positions: the producers stopped at them (full_x), and the MMAs of
+            // the slots' previous uses are done (empty), so the slots are free for the staged tile;
+            // with dequant warps, full_a keeps its one phase per position.
+            for (int k = 0; k < nstg; ++k) {
+                const bool here = mbar_wait(full_x(s), ph, abort_flag) && mbar_wait(empty(s), ph ^ 1u, abort_flag);
+                if (!__all_sync(0xffffffffu, here)) break;
+                if constexpr (kDequant)
+                    if (lane == 0) mbar_arrive(full_a(s));
+                ++g;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            // W4A8: the next tile's row factors, loaded now so that their latency hides behind this
+            // epilogue; stored after its barrier, once every thread has read this tile's
+            const bool next_rf = EPI == EPI_W4A8 && t + (int)gridDim.x < total && ri < BN;
+            const float2 nrf = next_rf ? row_factors(tile_of(t + gridDim.x).y * BN) : make_float2(0.f, 0.f);
+            // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
+            // The tile is written transposed into its staging slots as [m][128 n], then stored by
+            // one TMA store (the store warp) or copied out row by row with 16-byte stores.
+            bool ok = mbar_wait(acc_full, (uint32_t)tj & 1u, abort_flag) && !*abort_flag;
+            tc_fence_after();
             const bool has_ep = EPI != EPI_ACC && p.ep.any();
             const bool has_res = has_ep && p.ep.residual != nullptr;
-            // the residual tile, when it came in by TMA, sits where this thread stages its outputs:
+            // the residual tile, when it comes in by TMA, sits where this thread stages its outputs:
             // each element is read and then overwritten by the same thread
-            const bool res_smem = has_res && p.r_tma && mbar_wait(res_full, 0u, abort_flag);
+            const bool res_smem = has_res && p.r_tma;
             const bool res_glob = has_res && !p.r_tma;
-            const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
-            for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kAccCol + c0, v);
-                float rv[32];
-                if (res_glob) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int m = m_tile + c0 + i;
-                        rv[i] = (row < p.N && m < p.M) ? load_c<CDT>(p.ep.residual, (size_t)m * p.N + row) : 0.f;
+            if (ok && res_smem) ok = mbar_wait(res_full, (uint32_t)tj & 1u, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);   // the tensor-memory loads below are warp-collective
+            if (ok) {
+                float ws = 0.f, wo = 0.f;
+                if constexpr (EPI == EPI_W4A8) {
+                    if constexpr (G::kTable) {   // block-quantized W4A8 weights: dequantized per block already
+                        ws = 1.f;
+                        wo = 0.f;
+                    } else {                     // raw codes: the per-channel {offset, scale} here
+                        const float2 tt = __ldg(reinterpret_cast<const float2*>(p.T + tab_index(rc, 1, 0) * 2));
+                        wo = tt.x;
+                        ws = tt.y;
                     }
                 }
-                tmem_ld_wait();
-                if constexpr (EPI == EPI_ACC) {
+                // The fused epilogue: this thread's channel bias once, and per 32-column chunk the 32
+                // residual values (32 independent loads, one 64-byte segment of a residual row per
+                // warp each) before any of them is used; the activation is chosen once per chunk.
+                const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
+                for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kAccCol + c0, v);
+                    float rv[32];
+                    if (res_glob) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        reinterpret_cast<int32_t*>(tile)[(size_t)(c0 + i) * kBM + r] = __float2int_rn(__uint_as_float(v[i]));
-                } else {
-                    float y[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        y[i] = __uint_as_float(v[i]);
-                        if constexpr (EPI == EPI_W4A8) {
-                            // per-channel rescale, as * (ws * acc + wo * rowsum) =
-                            // ws * (as * acc) + wo * (as * rowsum): W4A8 (acc the exact integer
-                            // sum, see the file comment) and CODES8 (as = 1, rowsum = sum of a)
-                            const float2 f = rowf[c0 + i];   // the same row for the whole warp: a broadcast
-                            // with K split across blocks (CODES8), the offset term goes to split 0
-                            y[i] = fmaf(ws, f.x * y[i], blockIdx.z == 0 ? wo * f.y : 0.f);
+                        for (int i = 0; i < 32; ++i) {
+                            const int m = m_tile + c0 + i;
+                            rv[i] = (row < p.N && m < p.M) ? load_c<CDT>(p.ep.residual, (size_t)m * p.N + row) : 0.f;
                         }
                     }
-                    if (has_ep) {
+                    tmem_ld_wait();
+                    if constexpr (EPI == EPI_ACC) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) y[i] += bias_r;
-                        switch (p.ep.act) {
-                            case ACT_RELU:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_RELU>(y[i]);
-                                break;
-                            case ACT_SILU:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_SILU>(y[i]);
-                                break;
-                            case ACT_GELU_TANH:
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_GELU_TANH>(y[i]);
-                                break;
-                            default: break;
-                        }
-                        if (res_glob) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) y[i] += rv[i];
-                        } else if (res_smem) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) y[i] += load_s<CDT>(tile, (size_t)(c0 + i) * kBM + r);
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) store_c<CDT>(tile, (size_t)(c0 + i) * kBM + r, y[i]);
-                }
-            }
-        }
-        if (p.c_tma) {
-            // one TMA store of the staged tile (rows and channels past the end are not written);
-            // the block may retire once the store has read shared memory
-            ptx::fence_proxy_async_smem();
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-            if (ok && threadIdx.x == 64) {
-                if (EPI == EPI_ACC && p.acc_add)
-                    ptx::tma_reduce_add_3d(&maps.c, n_tile, m_tile, 0, smem_u32(tile));
-                else
-                    ptx::tma_store_3d(&maps.c, n_tile, m_tile, blockIdx.z, smem_u32(tile));
-                ptx::bulk_commit();
-                ptx::bulk_wait_read();
-            }
-        } else {
-        asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
-        if (ok) {
-            const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
-            constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
-            constexpr int kChunks = kBM / kPer;               // chunks per tile row
-            const bool add = EPI == EPI_ACC && p.acc_add;
-            uint8_t* out = (EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C)) +
-                           (add ? 0 : (size_t)blockIdx.z * p.M * p.N * kEsz);
-            const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-            for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
-                const int ml = idx / kChunks, c = idx - ml * kChunks;
-                const int n0 = c * kPer;
-                if (n0 >= nvalid) continue;
-                const uint8_t* src = tile + ((size_t)ml * kBM + n0) * kEsz;
-                uint8_t* dst = out + ((size_t)(m_tile + ml) * p.N + n_tile + n0) * kEsz;
-                if (add) {   // int32 accumulators of one K-chunk added in (exact, any order)
-                    for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
-                        atomicAdd(reinterpret_cast<int*>(dst) + e, reinterpret_cast<const int*>(src)[e]);
-                } else if (vec && n0 + kPer <= nvalid) {
-                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-                } else {
-                    for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
-                        for (int b = 0; b < kEsz; ++b) dst[e * kEsz + b] = src[e * kEsz + b];
-                }
-            }
-        }
-        }
-        // Params::rowmax: the max over the tile's channels of each staged row (the values as stored
-        // in C's type), read back from the staged tile after the epilogue warps' barrier that both
-        // branches above passed. Each lane owns one row and visits its 128 channels in 32 groups of
-        // 4, starting at group `lane` (the lanes of a warp then read different banks); the loads
-        // are independent, so the pass is a few hundred cycles. It only reads shared memory and may
-        // overlap the tile's TMA store.
-        if constexpr (EPI != EPI_ACC) {
-            const int ml = (warp - 2) * 32 + lane;
-            if (p.rowmax && ok && warp - 2 < BN / 32 && ml < min(BN, p.M - m_tile)) {
-                const int nvalid = min(kBM, p.N - n_tile);
-                float mx = 0.f;
-#pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const int c = 4 * ((j + lane) & 31);
-                    float v[4];
-                    if constexpr (kEsz == 4) {
-                        const float4 x = *reinterpret_cast<const float4*>(tile + ((size_t)ml * kBM + c) * 4);
-                        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+                        for (int i = 0; i < 32; ++i)
+                            reinterpret_cast<int32_t*>(tile)[(size_t)(c0 + i) * kBM + r] = __float2int_rn(__uint_as_float(v[i]));
                     } else {
-                        const uint2 x = *reinterpret_cast<const uint2*>(tile + ((size_t)ml * kBM + c) * 2);
-                        const uint32_t w[2] = {x.x, x.y};
+                        float y[32];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const unsigned short b = (unsigned short)(w[e >> 1] >> (16 * (e & 1)));
-                            v[e] = CDT == DT_F16 ? __half2float(__ushort_as_half(b)) : __uint_as_float((uint32_t)b << 16);
+                        for (int i = 0; i < 32; ++i) {
+                            y[i] = __uint_as_float(v[i]);
+                            if constexpr (EPI == EPI_W4A8) {
+                                // per-channel rescale, as * (ws * acc + wo * rowsum) =
+                                // ws * (as * acc) + wo * (as * rowsum): W4A8 (acc the exact integer
+                                // sum, see the file comment) and CODES8 (as = 1, rowsum = sum of a)
+                                const float2 f = rowf[c0 + i];   // the same row for the whole warp: a broadcast
+                                // with K split across blocks (CODES8), the offset term goes to split 0
+                                y[i] = fmaf(ws, f.x * y[i], blockIdx.z == 0 ? wo * f.y : 0.f);
+                            }
                         }
-                    }
+                        if (has_ep) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (c + e < nvalid) mx = fmaxf(mx, fabsf(v[e]));
+                            for (int i = 0; i < 32; ++i) y[i] += bias_r;
+                            switch (p.ep.act) {
+                                case ACT_RELU:
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_RELU>(y[i]);
+                                    break;
+                                case ACT_SILU:
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_SILU>(y[i]);
+                                    break;
+                                case ACT_GELU_TANH:
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) y[i] = act_fixed<ACT_GELU_TANH>(y[i]);
+                                    break;
+                                default: break;
+                            }
+                            if (res_glob) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) y[i] += rv[i];
+                            } else if (res_smem) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) y[i] += load_s<CDT>(tile, (size_t)(c0 + i) * kBM + r);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) store_c<CDT>(tile, (size_t)(c0 + i) * kBM + r, y[i]);
+                    }
                 }
-                p.rowmax[(size_t)n_idx * p.M + m_tile + ml] = mx;
+                // the accumulator has been read (tcgen05.wait::ld above): the next tile's MMAs may
+                // overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
             }
+            // the staged tile (and this thread's reads of the residual in it) before the store
+            // warp's TMA store and the copies that later reuse the slots
+            ptx::fence_proxy_async_smem();
+            // one decision for all epilogue warps: after an abort they leave the tile loop together
+            if (epi_any(!ok || *abort_flag != 0)) break;
+            if (next_rf) rowf[ri] = nrf;
+            if (!p.c_tma) {
+                const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
+                constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
+                constexpr int kChunks = kBM / kPer;               // chunks per tile row
+                const bool add = EPI == EPI_ACC && p.acc_add;
+                uint8_t* out = (EPI == EPI_ACC ? reinterpret_cast<uint8_t*>(p.acc) : static_cast<uint8_t*>(p.C)) +
+                               (add ? 0 : (size_t)blockIdx.z * p.M * p.N * kEsz);
+                const bool vec = ((size_t)p.N * kEsz) % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+                for (int idx = threadIdx.x - 64; idx < mvalid * kChunks; idx += kEpiThreads) {
+                    const int ml = idx / kChunks, c = idx - ml * kChunks;
+                    const int n0 = c * kPer;
+                    if (n0 >= nvalid) continue;
+                    const uint8_t* src = tile + ((size_t)ml * kBM + n0) * kEsz;
+                    uint8_t* dst = out + ((size_t)(m_tile + ml) * p.N + n_tile + n0) * kEsz;
+                    if (add) {   // int32 accumulators of one K-chunk added in (exact, any order)
+                        for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
+                            atomicAdd(reinterpret_cast<int*>(dst) + e, reinterpret_cast<const int*>(src)[e]);
+                    } else if (vec && n0 + kPer <= nvalid) {
+                        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+                    } else {
+                        for (int e = 0; e < kPer && n0 + e < nvalid; ++e)
+                            for (int b = 0; b < kEsz; ++b) dst[e * kEsz + b] = src[e * kEsz + b];
+                    }
+                }
+            }
+            // Params::rowmax: the max over the tile's channels of each staged row (the values as
+            // stored in C's type), read back from the staged tile. Each lane owns one row and visits
+            // its 128 channels in 32 groups of 4, starting at group `lane` (the lanes of a warp then
+            // read different banks); the loads are independent, so the pass is a few hundred cycles.
+            if constexpr (EPI != EPI_ACC) {
+                const int ml = (warp - 2) * 32 + lane;
+                if (p.rowmax && warp - 2 < BN / 32 && ml < min(BN, p.M - m_tile)) {
+                    const int nvalid = min(kBM, p.N - n_tile);
+                    float mx = 0.f;
+#pragma unroll 8
+                    for (int j = 0; j < 32; ++j) {
+                        const int c = 4 * ((j + lane) & 31);
+                        float v[4];
+                        if constexpr (kEsz == 4) {
+                            const float4 x = *reinterpret_cast<const float4*>(tile + ((size_t)ml * kBM + c) * 4);
+                            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+                        } else {
+                            const uint2 x = *reinterpret_cast<const uint2*>(tile + ((size_t)ml * kBM + c) * 2);
+                            const uint32_t w[2] = {x.x, x.y};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const unsigned short b = (unsigned short)(w[e >> 1] >> (16 * (e & 1)));
+                                v[e] = CDT == DT_F16 ? __half2float(__ushort_as_half(b)) : __uint_as_float((uint32_t)b << 16);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (c + e < nvalid) mx = fmaxf(mx, fabsf(v[e]));
+                    }
+                    p.rowmax[(size_t)n_idx * p.M + m_tile + ml] = mx;
+                }
+            }
+            // threads that read the staged tile above are done before the store warp hands its
+            // slots back to the producers
+            if (!p.c_tma || (EPI != EPI_ACC && p.rowmax)) asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+            // (the store warp took the previous tile: staged never runs two phases ahead of it)
+            if (threadIdx.x == 64 && (tj == 0 || mbar_wait(taken, (uint32_t)(tj - 1) & 1u, abort_flag)))
+                mbar_arrive(staged);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (*abort_flag) {
-            // After an abort the epilogue may not have waited for acc_full: the MMAs already issued
-            // finish before their tensor memory is released (acc_full is committed on every path).
-            volatile int never = 0;
-            ptx::mbar_wait(acc_full, 0u, &never, p.status);
-        }
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -910,33 +1071,49 @@ inline bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, in
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// SMs of the device current at the first call (thread-safe one-time initialization).
+inline int sm_count() {
+    static const int count = [] {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = kTargetSms;
+        return n;
+    }();
+    return count;
+}
+
+// The weight and table maps for the plan's sub-stages per stage, then the launch: one block per
+// tile, or (persistent form) at most one block per SM, each taking every gridDim.x-th tile.
 template <int WF, bool BF, int EPI, int CDT, int BN>
-cudaError_t launch_k(const Maps& maps, const Params& p, cudaStream_t s) {
-    auto kern = prefill_kernel<WF, BF, EPI, CDT, BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
+cudaError_t launch_k(Maps maps, Params p, cudaStream_t s) {
+    using T = Tiling<WF, BF, EPI, CDT, BN>;
+    using P = typename T::P;
+    cudaError_t e = make_wmap(&maps.w, p.Bp, WF, BF, p.N, p.K, P::kSub);
     if (e != cudaSuccess) return e;
-    dim3 grid(((p.N + kBM - 1) / kBM) * p.m_tiles, 1, p.splits);
+    p.tblocks = P::kSub < p.nb ? P::kSub : p.nb;
+    if constexpr (P::G::kTable) e = make_table_map(&maps.t, p.T, p.N, p.nb, p.tblocks);
+    else maps.t = maps.w;   // unused
+    if (e != cudaSuccess) return e;
+    auto kern = prefill_kernel<WF, BF, EPI, CDT, BN>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((p.N + kBM - 1) / kBM) * p.m_tiles;
+    const int blocks = T::kPersistent && tiles > sm_count() ? sm_count() : tiles;
+    dim3 grid(blocks, 1, p.splits);
     kern<<<grid, kThreads, kSmemMax, s>>>(maps, p);
     return cudaGetLastError();
 }
 
-// The weight and table maps for the plan's sub-stages per stage, then the launch for the output
-// type c_dtype (EPI_ACC: int32).
+// The raster for tile height BN, then the launch for the output type c_dtype (EPI_ACC: int32).
 template <int WF, bool BF, int EPI, int BN>
 cudaError_t launch_bn(Maps maps, Params p, int c_dtype, cudaStream_t s) {
-    using P = Plan<WF, BF, BN>;
-    cudaError_t e = make_wmap(&maps.w, p.Bp, WF, BF, p.N, p.K, P::kSub);
-    if (e != cudaSuccess) return e;
-    p.tblocks = P::kSub < p.nb ? P::kSub : p.nb;
     p.m_tiles = (p.M + BN - 1) / BN;
     // weights beyond half the L2 (measured: the 117 MB f16 weights of a 4096 x 14336 layer were read
     // about six times over with channel tiles fastest): row tiles fastest in groups of about two
     // waves of blocks
     const size_t wbytes = (size_t)p.N * p.K * WBox<WF>::kRowBytes / kBK;   // packed weight bytes
     p.group_n = wbytes > kL2GroupBytes ? ((2 * kTargetSms) / p.m_tiles > 1 ? (2 * kTargetSms) / p.m_tiles : 1) : 0;
-    if constexpr (P::G::kTable) e = make_table_map(&maps.t, p.T, p.N, p.nb, p.tblocks);
-    else maps.t = maps.w;   // unused
-    if (e != cudaSuccess) return e;
     if constexpr (EPI == EPI_ACC) return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
     switch (c_dtype) {
         case DT_F32: return launch_k<WF, BF, EPI, DT_F32, BN>(maps, p, s);
