@@ -232,3 +232,70 @@ def test_w4a8_block_weights_layer(M, K, N, block, a_dtype):
     assert np.array_equal(table_rows(T.cpu().numpy(), N, K // block), ref["T"])
     got = gpu_run(M, K, N, 3, block, A_np, a_dtype, Bp, T, synth.BF16)
     check_close(got, ref["R"], a_dtype, synth.BF16, f"w4a8 block {block}")
+
+
+# ---------------------------------------------------------------- persistent tiles
+# Blocks that run several tiles stage each output tile in ring slots that the pipeline reserves
+# after the tile's last stage. These cases run more tiles than the GPU has SMs, with a short wait
+# bound so that a pipeline that stalls fails within seconds instead of running out every wait.
+@pytest.fixture
+def short_waits():
+    prev = qg.qgemm_set_option(qg.OPT_WAIT_LIMIT_US, 200000)
+    yield
+    qg.qgemm_set_option(qg.OPT_WAIT_LIMIT_US, prev)
+    assert qg.qgemm_status() == 0
+
+
+def test_w4a8_long_k_many_tiles_exact(short_waits):
+    """The down-projection of the FFN pair, 2048 x 14336 -> 4096: int32 accumulator tiles (two
+    K-chunks added in int32) staged over two of the ring's three slots, 256 tiles on at most one
+    block per SM. Bit-exact at sampled points and on whole sampled rows."""
+    M, K, N = 2048, 14336, 4096
+    w, A_np, W_np = _w4a8_inputs(M, K, N, seed=5)
+    q, T = oracle.quantize(W_np, K, 15)
+    qa, s, rs = oracle.act_quant(oracle.values(A_np, w.a_dtype).astype(np.float32))
+    Bp, Tg = gpu_pack(W_np, 3, 0)
+    acc = _gpu_w4a8_acc(qa, Bp, M, K, N)
+    rng = np.random.default_rng(7)
+    mi, ni = rng.integers(0, M, 4096), rng.integers(0, N, 4096)
+    assert np.array_equal(acc[mi, ni], oracle.w4a8_acc_points(qa, q, mi, ni))
+    rows = np.sort(rng.choice(M, 8, replace=False))
+    acc_rows = oracle.w4a8_acc(qa[rows], q)
+    assert np.array_equal(acc[rows], acc_rows)
+    got = gpu_run(M, K, N, 3, 0, A_np, w.a_dtype, Bp, Tg, synth.BF16)
+    assert qg.qgemm_status() == 0
+    check_close(got[rows], oracle.w4a8_out(acc_rows, s[rows], rs[rows], T), w.a_dtype, synth.BF16, "w4a8 long K")
+
+
+@pytest.mark.parametrize("M,K,N,block,a_dtype", [
+    (2048, 4096, 14336, 0, synth.BF16),    # W4A8, 896 tiles of 256 rows
+    (1536, 1024, 2560, 64, synth.F16),     # Int4 prefill, 120 tiles: fewer than the SMs
+    (4096, 512, 4096, 64, synth.F16),      # Int4 prefill, short K (4 stages) over 512 tiles
+])
+def test_fused_epilogue_many_tiles(short_waits, M, K, N, block, a_dtype):
+    """Bias, activation and a residual tile brought in by TMA where the output is staged, on
+    blocks that run several tiles (rows sampled against the oracle)."""
+    mode = 3 if block == 0 else 1
+    w = synth.Workload("t", M, K, N, mode, block, a_dtype, synth.BF16, 11, 12)
+    A_np, W_np = synth.make_activations(w), synth.make_weights(w)
+    bias_np = synth.normal64(N, 13, stream=4, std=0.5).astype(np.float32)
+    res_np = synth.encode(synth.normal64(M * N, 14, stream=5).reshape(M, N), synth.BF16)
+    Bp, T = gpu_pack(W_np, mode, block)
+    A = torch_from(A_np, a_dtype)
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    res = torch_from(res_np, synth.BF16)
+    bias = torch.from_numpy(bias_np).to(DEV)
+    wsb = qg.qgemm_workspace_bytes(M, K, N, mode, block, a_dtype, synth.BF16)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    prev = qg.qgemm_set_option(qg.OPT_SPLIT_K, 0)
+    try:
+        qg.qgemm_run_fused(M, K, N, mode, block, A, a_dtype, Bp, T, bias, qg.ACT_SILU, res, C, synth.BF16, ws, wsb)
+        assert qg.qgemm_status() == 0
+    finally:
+        qg.qgemm_set_option(qg.OPT_SPLIT_K, prev)
+    rows = np.sort(np.random.default_rng(3).choice(M, 6, replace=False))
+    got = to_numpy_values(C, synth.BF16)[rows]
+    assert np.all(np.isfinite(got))
+    ref = oracle.reference_layer(mode, block, A_np[rows], a_dtype, W_np)
+    R = oracle.epilogue(ref["R"], bias_np, qg.ACT_SILU, oracle.values(res_np, synth.BF16)[rows])
+    check_close(got, R, a_dtype, synth.BF16, f"fused many tiles mode {mode}")

@@ -460,11 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     //       empty[S] (MMAs of the stage done) | acc_full (the tile's MMAs done) |
     //       res_full (the residual tile landed, Params::r_tma) | stall (Params::stall: never
     //       arrived at) | acc_empty (the epilogue warps have read the accumulator) |
-    //       staged (the output tile is staged) | taken (the store warp has taken it)
+    //       staged (the output tile is staged) | taken (the store warp has taken it) |
+    //       wt_staged (the weight producer has passed the tile's staging positions)
     // A barrier's waiter must never fall two phases behind it (a parity wait would then pass on
     // the wrong phase): every wait below is on a phase that cannot complete twice without the
     // waiter's own progress.
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 6);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 7);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
     float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
@@ -478,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t acc_empty = smem_u32(bars + 3 * kMaxStages + 3);
     const uint32_t staged = smem_u32(bars + 3 * kMaxStages + 4);
     const uint32_t taken = smem_u32(bars + 3 * kMaxStages + 5);
-    static_assert((3 * kMaxStages + 6) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
+    const uint32_t wt_staged = smem_u32(bars + 3 * kMaxStages + 6);
+    static_assert((3 * kMaxStages + 7) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
     constexpr uint32_t kTileBytes = (uint32_t)T::kTileBytes;
     // Staging positions after a tile whose stages end at position g_end: returns their count and
     // sets *slot to the first of the kSlots contiguous slots where the tile is staged (the
@@ -518,12 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tma_load_2d(st + t_off, &maps.t, 32 * ((ks * SUB) / bpb), tc.x * (kBM / 16), full_x(s));
     };
     // A producer lane's walk over the block's ring positions (the first one leaves before the
-    // block barrier): at a stage it waits for the slot's previous use, then `issue`s; at a staging
-    // position the activation producer (act) waits the same way and arrives on full_x without
-    // copies, the weight producer passes. The activation producer also brings in the residual tile
-    // (Params::r_tma) where the tile is staged, as soon as the staging slots' previous uses are
-    // done, so that its latency hides behind the tile's last stages. After an abort, the copies
-    // issued land before the block exits.
+    // block barrier): at every position it waits for the slot's previous use, then at a stage it
+    // `issue`s, at a staging position the activation producer (act) arrives on full_x without
+    // copies. The staging positions are released by the store warp, which does not wait for the
+    // weight producer otherwise: so that this producer never falls two phases behind a slot's
+    // empty barrier, it waits for the previous tile to be taken before the tile's staging
+    // positions and reports passing them (wt_staged), which the store warp waits for before it
+    // releases them. The activation producer also brings in the residual tile (Params::r_tma)
+    // where the tile is staged, as soon as the staging slots' previous uses are done, so that its
+    // latency hides behind the tile's last stages. After an abort, the copies issued land before
+    // the block exits.
     auto produce = [&](auto&& issue, bool act) {
         const bool res = act && EPI != EPI_ACC && p.r_tma;
         int g = 0, s = 0, tj = 0, res_issued = 0;
@@ -539,13 +545,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             int slot;
             const int np = nks + staging_of(g + nks, &slot);
             for (int i = 0; i < np; ++i) {
-                if (g > 0 && (i < nks || act)) {
+                if (!act && i == nks && tj > 0 && !mbar_wait(taken, (uint32_t)(tj - 1) & 1u, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (g > 0) {
                     if (*abort_flag || !mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
                         stop = true;
                         break;
                     }
                     if (i < nks) issue(tc, i, s);
-                    else mbar_arrive(full_x(s));
+                    else if (act) mbar_arrive(full_x(s));
                 }
                 real = i < nks ? real | (1u << s) : real & ~(1u << s);
                 ++g;
@@ -559,6 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     }
                     load_res(tc, slot);
                 }
+            }
+            if (!act && !stop) {
+                // (a tile without staging positions: still after the previous tile was taken)
+                if (np == nks && tj > 0 && !mbar_wait(taken, (uint32_t)(tj - 1) & 1u, abort_flag)) break;
+                mbar_arrive(wt_staged);
             }
         }
         if constexpr (!T::kPersistent) {
@@ -597,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(acc_empty, kEpiWarps);
         mbar_init(staged, 1);
         mbar_init(taken, 1);
+        mbar_init(wt_staged, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
@@ -635,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 int slot;
                 const int g_end = g + nks;
                 g = g_end + staging_of(g_end, &slot);
-                if (!mbar_wait(staged, (uint32_t)tj & 1u, abort_flag)) break;
+                if (!mbar_wait(staged, (uint32_t)tj & 1u, abort_flag) ||
+                    !mbar_wait(wt_staged, (uint32_t)tj & 1u, abort_flag))
+                    break;
                 mbar_arrive(taken);
                 if (p.c_tma) {
                     // rows and channels past the end are not written
