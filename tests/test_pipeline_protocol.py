@@ -2,7 +2,8 @@
 
 One block of the persistent tensor-core kernel (weight_quantized_gemm_gb300/csrc/prefill_kernel.cuh)
 is modelled as its roles -- the activation producer, the weight producer, the MMA issuer, the
-dequant / epilogue warps (one agent; thread 64 among them) and the store warp -- exchanging
+dequant / epilogue warps (two agents, one per column half of the tile; thread 64 in the first)
+and the store warp, which stores each 32-row slab as soon as its half has staged it -- exchanging
 arrivals on mbarriers with the hardware's phase-parity semantics: a wait for parity P passes as
 soon as the barrier's current phase has the other parity, which is only correct when the waiter
 is neither two phases behind nor waiting two phases ahead. Copies (TMA), MMA completion and store
@@ -17,6 +18,9 @@ ended. It is the protocol the kernel implements, restated; it does not run the k
 import random
 
 import pytest
+
+
+SLABS_PER_HALF = 4   # 32-row slabs per column half of a 256-row tile
 
 
 class Bar:
@@ -50,9 +54,12 @@ def run_block(S, k_slots, nks, tiles, residual, pre_stages=0, seed=0, delay=4):
     (finished, why)."""
     rnd = random.Random(seed)
     full_x = [Bar(1) for _ in range(S)]
-    full_a = [Bar(1) for _ in range(S)]
+    full_a = [Bar(2) for _ in range(S)]   # one arrival per epilogue agent (the kernel: per dequant warp)
     empty = [Bar(1) for _ in range(S)]
-    acc_full, acc_empty, staged, taken, res_full, wt_staged = (Bar(1) for _ in range(6))
+    acc_full, staged, taken, res_full, wt_staged = (Bar(1) for _ in range(5))
+    acc_empty = Bar(2)
+    slabs = [Bar(1) for _ in range(2 * SLABS_PER_HALF)]   # one arrival: the half's agent
+    half_done = Bar(2)   # both halves finished the tile's epilogue (the block's named barrier)
     events = []
     clock = [0]
     ended, landed, dequantized = set(), {}, set()
@@ -135,7 +142,7 @@ def run_block(S, k_slots, nks, tiles, residual, pre_stages=0, seed=0, delay=4):
                 if s == S:
                     s, ph = 0, ph ^ 1
 
-    def epilogue_warps():
+    def epilogue_warps(half):
         g = s = ph = 0
         pre = 0
         g_tile = 0
@@ -179,10 +186,16 @@ def run_block(S, k_slots, nks, tiles, residual, pre_stages=0, seed=0, delay=4):
             yield from wait(acc_full, tj & 1)
             if residual:
                 yield from wait(res_full, tj & 1)
-            acc_empty.arrive()
             if tj > 0:
-                yield from wait(taken, (tj - 1) & 1)   # thread 64, before it arrives on staged
-            staged.arrive()
+                yield from wait(taken, (tj - 1) & 1)   # before this tile's first slab
+            for k in range(SLABS_PER_HALF):
+                slabs[half * SLABS_PER_HALF + k].arrive()
+                yield "step"
+            acc_empty.arrive()
+            half_done.arrive()
+            yield from wait(half_done, tj & 1)   # the epilogue warps' barrier
+            if half == 0:
+                staged.arrive()   # thread 64 (the taken wait above already covered it)
             yield "step"
 
     def store_warp():
@@ -191,6 +204,9 @@ def run_block(S, k_slots, nks, tiles, residual, pre_stages=0, seed=0, delay=4):
             g_end = g + nks
             _, staging = staging_of(g_end)
             g = g_end + staging
+            for kk in range(SLABS_PER_HALF):
+                for hh in range(2):
+                    yield from wait(slabs[hh * SLABS_PER_HALF + kk], tj & 1)
             yield from wait(staged, tj & 1)
             yield from wait(wt_staged, tj & 1)
             taken.arrive()
@@ -199,7 +215,7 @@ def run_block(S, k_slots, nks, tiles, residual, pre_stages=0, seed=0, delay=4):
             yield "step"
 
     roles = {"act": producer(True), "wt": producer(False), "mma": mma(),
-             "epilogue": epilogue_warps(), "store": store_warp()}
+             "epilogue0": epilogue_warps(0), "epilogue1": epilogue_warps(1), "store": store_warp()}
     alive, idle = set(roles), 0
     while alive:
         clock[0] += 1

@@ -96,7 +96,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.A, bf, a.M, a.K, p.BN);
     if (e != cudaSuccess) return e;
-    p.c_tma = pf::make_out_map(&maps.c, p.C, kdt, a.M, a.N, p.BN, p.splits) ? 1 : 0;
+    p.c_tma = pf::make_out_map(&maps.c, p.C, kdt, a.M, a.N, pf::kSlabRows, p.splits) ? 1 : 0;
     if (!p.c_tma) maps.c = maps.a;             // unused
     p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), kdt, a.M, a.N, p.BN, 1) ? 1 : 0;
     if (!p.r_tma) maps.r = maps.a;             // unused

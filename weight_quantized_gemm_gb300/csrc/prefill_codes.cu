@@ -66,8 +66,8 @@ cudaError_t launch_w4a8_gemm(const W4A8Args& a, cudaStream_t s) {
     pf::Maps maps;
     cudaError_t e = pf::make_tmap(&maps.a, a.qa16, false, a.M, a.K, p.BN);
     if (e != cudaSuccess) return e;
-    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, p.BN, 1) ? 1 : 0)
-                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, p.BN, 1) ? 1 : 0);
+    p.c_tma = a.acc ? (pf::make_out_map(&maps.c, a.acc, -1, a.M, a.N, pf::kSlabRows, 1) ? 1 : 0)
+                    : (pf::make_out_map(&maps.c, a.C, a.c_dtype, a.M, a.N, pf::kSlabRows, 1) ? 1 : 0);
     if (!p.c_tma) maps.c = maps.a;     // unused
     p.r_tma = p.ep.residual && pf::make_out_map(&maps.r, const_cast<void*>(p.ep.residual), a.c_dtype, a.M, a.N, p.BN, 1)
                   ? 1 : 0;

@@ -322,7 +322,9 @@ __device__ __forceinline__ void store_c(void* C, size_t idx, float v) {
 // One stage is one round of the pipeline's barriers, so SUB = 2 halves the waits, arrivals and
 // commits per unit of K; the ring holds as many stages as shared and tensor memory allow.
 constexpr size_t kSmemMax = 232448;                 // opt-in shared memory per block
-constexpr int kTail = 256 + kMaxBN * 8;              // barriers + W4A8 row factors after the ring
+constexpr int kTail = 512 + kMaxBN * 8;              // barriers + W4A8 row factors after the ring
+constexpr int kSlabRows = 32;                         // rows of A per TMA store of a staged tile
+constexpr int kMaxSlabs = kMaxBN / kSlabRows;
 constexpr int kRing = (int)kSmemMax - kTail;         // bytes for the stages
 constexpr int kMaxStages = 8;
 constexpr size_t kL2GroupBytes = 64u << 20;         // weights above this take the grouped raster
@@ -461,14 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     //       res_full (the residual tile landed, Params::r_tma) | stall (Params::stall: never
     //       arrived at) | acc_empty (the epilogue warps have read the accumulator) |
     //       staged (the output tile is staged) | taken (the store warp has taken it) |
-    //       wt_staged (the weight producer has passed the tile's staging positions)
+    //       wt_staged (the weight producer has passed the tile's staging positions) |
+    //       slab[BN / 32] (rows [32 k, 32 k + 32) of the tile are staged: one arrival per warp
+    //       of the epilogue's column half that writes them)
     // A barrier's waiter must never fall two phases behind it (a parity wait would then pass on
     // the wrong phase): every wait below is on a phase that cannot complete twice without the
     // waiter's own progress.
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 7);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 7 + kMaxSlabs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
-    float2* rowf = reinterpret_cast<float2*>(smem + kRing + 256);
+    float2* rowf = reinterpret_cast<float2*>(smem + kRing + 512);
     const uint32_t st_s = smem_u32(smem);
     auto full_x = [&](int s) { return smem_u32(bars + s); };
     auto full_a = [&](int s) { return smem_u32(bars + kMaxStages + s); };
@@ -480,7 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t staged = smem_u32(bars + 3 * kMaxStages + 4);
     const uint32_t taken = smem_u32(bars + 3 * kMaxStages + 5);
     const uint32_t wt_staged = smem_u32(bars + 3 * kMaxStages + 6);
-    static_assert((3 * kMaxStages + 7) * 8 + 8 <= 256, "barriers, TMEM slot and abort flag fit the tail");
+    auto slab = [&](int k) { return smem_u32(bars + 3 * kMaxStages + 7 + k); };
+    constexpr int kSlabs = BN / kSlabRows;
+    static_assert((3 * kMaxStages + 7 + kMaxSlabs) * 8 + 8 <= 512, "barriers, TMEM slot and abort flag fit the tail");
     constexpr uint32_t kTileBytes = (uint32_t)T::kTileBytes;
     // Staging positions after a tile whose stages end at position g_end: returns their count and
     // sets *slot to the first of the kSlots contiguous slots where the tile is staged (the
@@ -613,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         mbar_init(staged, 1);
         mbar_init(taken, 1);
         mbar_init(wt_staged, 1);
+        for (int k = 0; k < kSlabs; ++k) mbar_init(slab(k), 4);   // the 4 warps of a column half
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         ptx::prefetch_tmap(&maps.a);
@@ -643,31 +650,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ---------------- TMA producer of the activation boxes
         if (lane == 0) produce(issue_act, true);
     } else if (warp == kStoreWarp) {
-        // ---------------- the staged tiles out (one TMA store each), then their staging positions
-        // released to the producers
+        // ---------------- the staged tiles out, 32 rows per TMA store as soon as they are staged
+        // (the stores read shared memory while the epilogue still works on later rows), then
+        // the staging positions released to the producers
         if (lane == 0) {
+            constexpr uint32_t kEsz = (EPI == EPI_ACC || CDT == DT_F32) ? 4u : 2u;
             int g = 0;
-            for (int t = blockIdx.x, tj = 0; t < total; t += gridDim.x, ++tj) {
+            bool stop = false;
+            for (int t = blockIdx.x, tj = 0; t < total && !stop; t += gridDim.x, ++tj) {
                 int slot;
                 const int g_end = g + nks;
                 g = g_end + staging_of(g_end, &slot);
+                const uint32_t stile = st_s + (uint32_t)slot * SB;
+                if (p.c_tma) {
+                    const int2 tc = tile_of(t);
+                    // the two column halves of the epilogue stage their slabs side by side
+                    for (int kk = 0; kk < kSlabs / 2 && !stop; ++kk) {
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int k = hh * (kSlabs / 2) + kk;
+                            if (!mbar_wait(slab(k), (uint32_t)tj & 1u, abort_flag)) {
+                                stop = true;
+                                break;
+                            }
+                            // rows and channels past the end are not written
+                            const uint32_t src = stile + (uint32_t)k * kSlabRows * kBM * kEsz;
+                            if (EPI == EPI_ACC && p.acc_add)
+                                ptx::tma_reduce_add_3d(&maps.c, tc.x * kBM, tc.y * BN + k * kSlabRows, 0, src);
+                            else
+                                ptx::tma_store_3d(&maps.c, tc.x * kBM, tc.y * BN + k * kSlabRows, blockIdx.z, src);
+                            ptx::bulk_commit();
+                        }
+                    }
+                    if (stop) break;
+                }
                 if (!mbar_wait(staged, (uint32_t)tj & 1u, abort_flag) ||
                     !mbar_wait(wt_staged, (uint32_t)tj & 1u, abort_flag))
                     break;
                 mbar_arrive(taken);
-                if (p.c_tma) {
-                    // rows and channels past the end are not written
-                    const int2 tc = tile_of(t);
-                    const uint32_t stile = st_s + (uint32_t)slot * SB;
-                    if (EPI == EPI_ACC && p.acc_add)
-                        ptx::tma_reduce_add_3d(&maps.c, tc.x * kBM, tc.y * BN, 0, stile);
-                    else
-                        ptx::tma_store_3d(&maps.c, tc.x * kBM, tc.y * BN, blockIdx.z, stile);
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_read();
-                }
+                ptx::bulk_wait_read();
                 for (int k = g_end; k < g; ++k) mbar_arrive(empty(k % S));   // the staging positions
             }
+            ptx::bulk_wait_read();   // (after an abort: the stores issued have read shared memory)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer. tcgen05.mma issue stalls while the tensor pipe's queue is
@@ -853,6 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 // residual values (32 independent loads, one 64-byte segment of a residual row per
                 // warp each) before any of them is used; the activation is chosen once per chunk.
                 const float bias_r = (p.ep.bias && row < p.N) ? __ldg(p.ep.bias + row) : 0.f;
+                // (the store warp took the previous tile: the slab barriers never run two phases
+                // ahead of it)
+                if (p.c_tma && tj > 0 && lane == 0) mbar_wait(taken, (uint32_t)(tj - 1) & 1u, abort_flag);
                 for (int c0 = h * (BN / 2); c0 < (h + 1) * (BN / 2); c0 += 32) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + kAccCol + c0, v);
@@ -911,6 +937,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                         }
 #pragma unroll
                         for (int i = 0; i < 32; ++i) store_c<CDT>(tile, (size_t)(c0 + i) * kBM + r, y[i]);
+                    }
+                    if (p.c_tma) {   // these 32 rows are staged by this warp: visible to the store
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(slab(c0 / kSlabRows));
                     }
                 }
                 // the accumulator has been read (tcgen05.wait::ld above): the next tile's MMAs may
@@ -1070,10 +1101,11 @@ inline cudaError_t make_table_map(CUtensorMap* map, const float* T, int N, int n
 }
 
 // The output [depth][M][N] (bf16 / f16 / f32, or int32 accumulators; depth = the K-splits' partial
-// sums, else 1) as a 3-D tensor; box = one tile of 128 channels x BN rows of one slice, matching the
-// staged [rows][128] tile. Only when a row is a whole number of 16-byte units (TMA strides) and
-// the base is 16-byte aligned; else returns false.
-inline bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int BN, int depth) {
+// sums, else 1) as a 3-D tensor; box = 128 channels x box_rows rows of one slice, matching the staged
+// [rows][128] tile (the output: one 32-row slab per store; the residual: the whole tile). Only when
+// a row is a whole number of 16-byte units (TMA strides) and the base is 16-byte aligned; else
+// returns false.
+inline bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, int box_rows, int depth) {
     const size_t esz = kind == DT_F32 || kind < 0 ? 4 : 2;
     if (((size_t)N * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return false;
     EncodeTiledFn enc = tensor_map_encoder();
@@ -1083,7 +1115,7 @@ inline bool make_out_map(CUtensorMap* map, void* out, int kind, int M, int N, in
                                    : (kind == DT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16));
     const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)depth};
     const cuuint64_t strides[2] = {(cuuint64_t)N * esz, (cuuint64_t)M * N * esz};
-    const cuuint32_t box[3] = {(cuuint32_t)kBM, (cuuint32_t)BN, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)kBM, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, dt, 3, out, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
