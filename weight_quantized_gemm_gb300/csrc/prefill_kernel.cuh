@@ -224,6 +224,13 @@ __device__ __forceinline__ void fma2(float x0, float x1, float s, float c0, floa
         : "=f"(r0), "=f"(r1)
         : "f"(x0), "f"(x1), "f"(s), "f"(c0), "f"(c1));
 }
+// (x0, x1) * (y0, y1) in one packed float32 instruction
+__device__ __forceinline__ void mul2(float x0, float x1, float y0, float y1, float& r0, float& r1) {
+    asm("{\n\t.reg .b64 x, y, d;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, x, y;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
 // byte j of w moved to bits 15..22
 template <int J>
 __device__ __forceinline__ uint32_t byte_to_15(uint32_t w) {
@@ -471,8 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // waiter's own progress.
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 7 + kMaxSlabs);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // W4A8: per row m of the tile {as[m], as[m] * rowsum[m]} (the row factors of the epilogue)
-    float2* rowf = reinterpret_cast<float2*>(smem + kRing + 512);
+    // W4A8: per row m of the tile as[m] and as[m] * rowsum[m] (the row factors of the epilogue),
+    // as two arrays so that two rows' factors load as one pair
+    float* rf_as = reinterpret_cast<float*>(smem + kRing + 512);
+    float* rf_ars = rf_as + kMaxBN;
     const uint32_t st_s = smem_u32(smem);
     auto full_x = [&](int s) { return smem_u32(bars + s); };
     auto full_a = [&](int s) { return smem_u32(bars + kMaxStages + s); };
@@ -782,7 +791,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if constexpr (EPI == EPI_W4A8) {
                 // the first tile's row factors while its first stages are in flight (later tiles'
                 // were stored after the previous epilogue's barrier)
-                if (tj == 0 && ri < BN) rowf[ri] = row_factors(m_tile);
+                if (tj == 0 && ri < BN) {
+                    const float2 f = row_factors(m_tile);
+                    rf_as[ri] = f.x;
+                    rf_ars[ri] = f.y;
+                }
                 asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");   // the epilogue warps only
             }
             if constexpr (kDequant) {
@@ -898,15 +911,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     } else {
                         float y[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            y[i] = __uint_as_float(v[i]);
-                            if constexpr (EPI == EPI_W4A8) {
-                                // per-channel rescale, as * (ws * acc + wo * rowsum) =
-                                // ws * (as * acc) + wo * (as * rowsum): W4A8 (acc the exact integer
-                                // sum, see the file comment) and CODES8 (as = 1, rowsum = sum of a)
-                                const float2 f = rowf[c0 + i];   // the same row for the whole warp: a broadcast
-                                // with K split across blocks (CODES8), the offset term goes to split 0
-                                y[i] = fmaf(ws, f.x * y[i], blockIdx.z == 0 ? wo * f.y : 0.f);
+                        for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(v[i]);
+                        if constexpr (EPI == EPI_W4A8) {
+                            // per-channel rescale, as * (ws * acc + wo * rowsum) =
+                            // fma(ws, as * acc, wo * (as * rowsum)): W4A8 (acc the exact integer sum,
+                            // see the file comment) and CODES8 (as = 1, rowsum = sum of a); two rows
+                            // per packed instruction, each rounded as the scalar steps would be. The
+                            // row factors are the same for the whole warp: broadcast loads. With K
+                            // split across blocks (CODES8), the offset term goes to split 0.
+                            const bool off = blockIdx.z == 0;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float2 a2 = *reinterpret_cast<const float2*>(rf_as + c0 + i);
+                                const float2 r2 = *reinterpret_cast<const float2*>(rf_ars + c0 + i);
+                                float t0, t1, u0 = 0.f, u1 = 0.f;
+                                mul2(a2.x, a2.y, y[i], y[i + 1], t0, t1);
+                                if (off) mul2(wo, wo, r2.x, r2.y, u0, u1);
+                                fma2(t0, t1, ws, u0, u1, y[i], y[i + 1]);
                             }
                         }
                         if (has_ep) {
@@ -955,7 +976,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             ptx::fence_proxy_async_smem();
             // one decision for all epilogue warps: after an abort they leave the tile loop together
             if (epi_any(!ok || *abort_flag != 0)) break;
-            if (next_rf) rowf[ri] = nrf;
+            if (next_rf) {
+                rf_as[ri] = nrf.x;
+                rf_ars[ri] = nrf.y;
+            }
             if (!p.c_tma) {
                 const int nvalid = min(kBM, p.N - n_tile), mvalid = min(BN, p.M - m_tile);
                 constexpr int kPer = 16 / kEsz;                   // elements per 16-byte chunk
