@@ -6,16 +6,20 @@
 // «为什么用 Conv1x1 来测 GEMM») is computed transposed, D[n][m] = sum_k W[n][k] * A[m][k], so that
 // the operand that needs work before it can be multiplied -- the packed weight -- is the MMA's
 // A operand and lives in tensor memory, while the activations stream in by TMA:
-//   - a TMA warp loads, per pipeline stage, the stage's K slice of A (up to 256 rows, 128-byte
-//     swizzle), the packed weight rows of the 128-channel tile and their {offset, scale} table
-//     entries into shared memory; a stage is one or two 64-wide sub-stages of K;
+//   - two TMA producer warps load, per pipeline stage, the stage's K slice of A (up to 256 rows,
+//     128-byte swizzle) and the packed weight rows of the 128-channel tile with their {offset,
+//     scale} table entries into shared memory; a stage is one or two 64-wide sub-stages of K;
 //   - dequant warps rebuild w = q * scale + offset in float32 (one rounding to the activation's
 //     16-bit type) and write them into a TMEM stage with tcgen05.st;
 //   - one thread issues tcgen05.mma (kind::f16, M = 128, N = tile rows of A, K = 16 per
 //     instruction) with A from TMEM and B from shared memory, accumulating in TMEM, and
 //     commits each stage back to the producers;
-//   - after the last stage the dequant warps read the accumulator with tcgen05.ld, stage the
-//     tile in shared memory and store it (one TMA store where the rows allow).
+//   - after the last stage the dequant warps read the accumulator with tcgen05.ld and stage the
+//     tile in ring slots reserved for it; a store warp writes it out by TMA, 32 rows per store
+//     as soon as they are staged (where the rows allow), then hands the slots back.
+// Blocks are persistent where the staging leaves the ring a slot for the next tile: at most one
+// per SM, each running through a sequence of tiles while the ring's stages and barrier phases run
+// on (see the kernel's own comment).
 // Shapes whose tiles fill less than one wave of SMs split K across blocks (grid z): each split
 // writes float32 partial sums and a second kernel adds them in a fixed order.
 // W4A8 ("W4 解包为 INT8 ... S8×S8→S32", «测试用例与注册机制») uses the same kernel with the 4-bit
@@ -80,7 +84,7 @@ struct Params {
     int32_t* acc;             // EPI_ACC output
     int acc_add;              // EPI_ACC: add the tile into acc (int32, exact) instead of storing it; the
                               // K-splits then all add into the one [M][N] array
-    int c_tma;                // the output tile goes out by one TMA store (else 16-byte row stores)
+    int c_tma;                // the output tile goes out by TMA stores of 32 rows (else 16-byte row stores)
     int r_tma;                // the epilogue's residual tile comes in by one TMA load (Maps::r)
     int splits;               // K-splits (grid z): split z writes float32 partial sums to C + z M N
     int tblocks;              // K-blocks per table box (min(SUB, nb))
@@ -862,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const float2 nrf = next_rf ? row_factors(tile_of(t + gridDim.x).y * BN) : make_float2(0.f, 0.f);
             // ---------------- epilogue: this warp's lane quarter, columns [h BN/2, (h+1) BN/2).
             // The tile is written transposed into its staging slots as [m][128 n], then stored by
-            // one TMA store (the store warp) or copied out row by row with 16-byte stores.
+            // TMA stores of 32 rows (the store warp) or copied out row by row with 16-byte stores.
             bool ok = mbar_wait(acc_full, (uint32_t)tj & 1u, abort_flag) && !*abort_flag;
             tc_fence_after();
             const bool has_ep = EPI != EPI_ACC && p.ep.any();
